@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan hot path on B300.
+
+One step = one ssm_scan_fwd over the Mamba-1.4B layer workload with its fused front end
+(batch 8, d_inner 4096, d_state 16, L 2048, bf16 in/out, fp32 state): causal conv1d + SiLU,
+softplus step, zero-order-hold discretisation, scan, C readout, D skip and SiLU gate, all in one
+kernel launch.  Inputs are seeded synthetic tensors resident in HBM before the timed region.
+
+Prints ONE JSON line (rank 0).  Keys beyond the base contract:
+  roofline      dominant kernel vs its ALU (MUFU) roof: algorithmic transcendental ops per launch
+                / CUDA-event launch time, against 148 SMs x measured ex2 rate/clk x max SM clock
+  hbm           the same launch against the measured HBM copy bandwidth
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload, host cores
+  e2e           the same metric through the public API with pinned host buffers, copies included
+  decode        the constant-state decode workload (ssm_state_update, 64 layers x 128 tokens)
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no data-path collective); the
+reported value is the elements of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+WORKLOAD = "mamba1.4b_conv"
+METRIC = "scan elems/s (B*D*L*N)"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6400.0
+MAX_SM_MHZ = 2032.0
+
+
+# ---------------------------------------------------------------------------------------------
+# accounting (per unit = one (b, d, t) of the scan)
+# ---------------------------------------------------------------------------------------------
+def scan_bytes(cfg) -> int:
+    """Algorithmic HBM bytes of one scan launch: u/x, delta, z read and y written once per (b, d, t),
+    B and C once per (b, n, t), per-channel parameters once, final state written once."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    bdl = cfg.batch * cfg.dim * cfg.seqlen
+    per_bdl = e * (2 + (1 if cfg.has_z else 0) + 1)
+    bc = 2 * cfg.batch * cfg.dstate * cfg.seqlen * e
+    params = 4 * cfg.dim * (cfg.dstate + 2 + (5 if cfg.conv else 0))
+    state = 4 * cfg.batch * cfg.dim * cfg.dstate
+    return bdl * per_bdl + bc + params + state
+
+
+def scan_mufu_ops(cfg) -> int:
+    """Transcendental operations the scan requires per (b, d, t): N exponentials for Abar, softplus
+    (exp + log), the gate's sigmoid (exp + reciprocal) and, with the fused conv, its SiLU sigmoid
+    (exp + reciprocal)."""
+    per = cfg.dstate + 2 + (2 if cfg.has_z else 0) + (2 if cfg.conv else 0)
+    return per * cfg.batch * cfg.dim * cfg.seqlen
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p))
+        except Exception:
+            pass
+    return {}
+
+
+def mufu_rate_per_clk(device_ok: bool) -> tuple:
+    """ex2 results per clock per SM: measured by bench_peaks.cu when it builds and runs, else 32 (the
+    rate measured on the B300s)."""
+    if device_ok:
+        exe = os.path.join(ROOT, "bench_peaks")
+        src = os.path.join(ROOT, "bench_peaks.cu")
+        try:
+            if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
+                subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src],
+                               check=True, capture_output=True, timeout=300)
+            out = subprocess.run([exe], capture_output=True, text=True, timeout=120).stdout.strip().splitlines()[-1]
+            j = json.loads(out)
+            return float(j["per_clk_per_sm"]["ex2"]), j
+        except Exception as e:  # keep the benchmark running; say where the number came from
+            return 32.0, {"error": str(e)}
+    return 32.0, {}
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        t1 = getattr(self, "t1", time.time())
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if self.t0 - 0.05 <= ts <= t1 + 0.05] or [p for _, p in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        mhz = [float(p[1]) for p in inside if p[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": float(inside[0][2]) if inside[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max((float(p[3]) for p in inside if p[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (timing only: barrier + max over ranks, no data-path collective)
+# ---------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_batches(total_ranks: int, rank: int, per_rank_batch: int):
+    """Weak scaling: rank r owns global batch rows [r * per_rank_batch, (r + 1) * per_rank_batch)."""
+    return range(rank * per_rank_batch, (rank + 1) * per_rank_batch)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU baseline (the oracle as it stands, bounded sample, host cores)
+# ---------------------------------------------------------------------------------------------
+def oracle_rate(d: dict, target_s: float, seed: int = 0):
+    """Runs the fp64 oracle on a growing sample of (b, d) rows until one run takes >= target_s/4, then
+    once more sized for about target_s.  Returns (elements/s, threads, rows, seconds)."""
+    import numpy as np
+    import oracle
+    Bsz, D, L = d["u"].shape
+    N = d["A"].shape[1]
+    rng = np.random.default_rng(seed)
+    allrows = [(int(b), int(c)) for b, c in zip(rng.integers(0, Bsz, 1 << 16), rng.integers(0, D, 1 << 16))]
+    R = 16
+    while True:
+        t = time.time()
+        _, _, nt = oracle.scan(d, rows=allrows[:R])
+        dt = time.time() - t
+        if dt >= target_s / 4 or R >= len(allrows):
+            break
+        R = min(len(allrows), R * 4)
+    R2 = max(1, min(len(allrows), int(R * target_s / max(dt, 1e-6))))
+    t = time.time()
+    _, _, nt = oracle.scan(d, rows=allrows[:R2])
+    dt = time.time() - t
+    return R2 * L * N / dt, nt, R2, dt
+
+
+# ---------------------------------------------------------------------------------------------
+# the b300 arm
+# ---------------------------------------------------------------------------------------------
+def run_b300(args, rank, world, local):
+    import selective_state_space_156_b300 as ssm
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workloads.SCAN_CONFIGS[args.workload]
+    cpu_inputs = workloads.make_scan_inputs(cfg, seed=cfg.seed + 7919 * rank)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu_inputs.items()}
+    y = torch.empty_like(g["u"])
+    h_out = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+    nws = ssm.ssm_scan_workspace_size(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], Dskip=g["Dskip"],
+                                      delta_bias=g["delta_bias"], z=g["z"], conv_w=g["conv_w"], conv_b=g["conv_b"],
+                                      h_out=h_out, y=y)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if nws > 0 else 1
+
+    def step():
+        ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], Dskip=g["Dskip"], delta_bias=g["delta_bias"],
+                         z=g["z"], conv_w=g["conv_w"], conv_b=g["conv_b"], h_out=h_out, y=y, workspace=ws)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        for i in range(K):
+            flush.zero_()                 # L2 flush between timed steps, outside the events
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.time() - wall0
+        clk.mark_end()
+    times = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms_local = statistics.fmean(times)
+    ms = max_over_ranks(ms_local, world)
+    elements = cfg.elements
+    value = world * elements / (ms * 1e-3)
+
+    # --- end to end through the public API with pinned host buffers ---
+    e2e = None
+    if not args.no_e2e:
+        names = ["u", "delta", "z", "Bm", "Cm", "A", "Dskip", "delta_bias", "conv_w", "conv_b"]
+        host = {k: cpu_inputs[k].pin_memory() for k in names}
+        devb = {k: torch.empty_like(host[k], device=dev) for k in names}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            for k in names:
+                devb[k].copy_(host[k], non_blocking=True)
+            ssm.ssm_scan_fwd(devb["u"], devb["delta"], devb["A"], devb["Bm"], devb["Cm"], Dskip=devb["Dskip"],
+                             delta_bias=devb["delta_bias"], z=devb["z"], conv_w=devb["conv_w"], conv_b=devb["conv_b"],
+                             y=y, workspace=ws)
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        E = max(3, min(args.e2e_steps, K))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(E):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / E, world)
+        e2e = {"value": world * elements / (e2e_ms * 1e-3), "unit": "elem/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
+
+    # --- roofline of the dominant (only) kernel ---
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or FALLBACK_HBM_GBS
+    rate_clk, probe = mufu_rate_per_clk(True) if rank == 0 else (32.0, {})
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mufu_peak = sms * rate_clk * MAX_SM_MHZ * 1e6           # ex2-class ops / s
+    mufu_ops = scan_mufu_ops(cfg)
+    nbytes = scan_bytes(cfg)
+    t_s = ms * 1e-3
+    roof = {"bound": "alu", "achieved": mufu_ops / t_s / 1e12, "peak": mufu_peak / 1e12, "unit": "Tmufu/s",
+            "frac": (mufu_ops / t_s) / mufu_peak, "traffic": args.traffic,
+            "peak_source": f"derived: {sms} SMs x {rate_clk:.1f} ex2/clk/SM (bench_peaks.cu) x {MAX_SM_MHZ:.0f} MHz",
+            "ops_per_launch": mufu_ops, "kernel": "scan_seq_kernel (final pass)"}
+    hbm = {"achieved_gbs": nbytes / t_s / 1e9, "peak_gbs": hbm_peak, "frac": nbytes / t_s / 1e9 / hbm_peak,
+           "bytes_per_launch": nbytes, "peak_source": hbm_src}
+
+    # --- decode workload (ssm_state_update) ---
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(ssm, dev, hbm_peak, world)
+
+    # --- CPU baseline: oracle on host cores, rank 0 at N = 1 only ---
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rate, nt, R, secs = oracle_rate(cpu_inputs, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "elem/s", "cores": nt, "kind": "oracle",
+               "sample": f"{R} random (b, d) rows of {cfg.batch * cfg.dim}, full L={cfg.seqlen}, N={cfg.dstate} "
+                         f"({secs:.1f} s, fp64 C, one thread per row)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} "
+                                   f"L={cfg.seqlen} bf16 I/O, fp32 state, fused conv1d(k=4)+SiLU, ZOH, D skip, "
+                                   "SiLU(z) gate", "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
+                       "parallelism": f"replicas x{world} (batch shards, no collective)",
+                       "l2": "256 MB buffer written between timed steps, outside the events; inputs 538 MB"},
+            "gpu_launches": K * launches_per_step,
+            "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+            "clocks": clk.summary(), "wall_s_timed_region": wall, "mufu_probe": probe,
+            "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_decode(ssm, dev, hbm_peak, world, steps=None):
+    """64 layers x 128 tokens of ssm_state_update, layer-major per token, replayed as one CUDA graph per
+    token.  Every layer keeps its own fp32 state cache (5.4 GB in total); per-token inputs come from a
+    pool of 64 sets (512 MB), so neither states nor inputs can stay in L2 between uses."""
+    cfg = workloads.DECODE_CONFIG
+    P = 64
+    steps = steps or cfg.steps
+    pool = workloads.make_decode_pool(cfg, P, device=dev)
+    layers = [workloads.make_decode_layer(cfg, l, device=dev) for l in range(cfg.layers)]
+    y = torch.empty((cfg.batch, cfg.dim), dtype=torch.bfloat16, device=dev)
+
+    def token(step):
+        for l in range(cfg.layers):
+            k = workloads.decode_pool_index(l, step, P)
+            L_ = layers[l]
+            ssm.ssm_state_update(L_["state"], pool["u"][k], pool["delta"][k], L_["A"], pool["Bm"][k], pool["Cm"][k],
+                                 Dskip=L_["Dskip"], delta_bias=L_["delta_bias"], z=pool["z"][k], y=y)
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(s):
+        token(0)  # warm-up outside capture
+        for gi in range(P):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                token(gi)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for st in range(steps):
+        graphs[st % P].replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    ms = max_over_ranks(ms, world)
+    state_bytes = cfg.batch * cfg.dim * cfg.dstate * 4
+    per_call = 2 * state_bytes + 3 * cfg.batch * cfg.dim * 2 + 2 * cfg.batch * cfg.dstate * 2 + \
+        cfg.batch * cfg.dim * 2 + cfg.dim * (cfg.dstate + 2) * 4
+    calls = steps * cfg.layers
+    gbs = per_call * calls / (ms * 1e-3) / 1e9
+    return {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} x {cfg.layers} layers "
+                        f"x {steps} tokens, bf16 I/O, fp32 state cache updated in place",
+            "tokens_per_s": world * cfg.batch * steps / (ms * 1e-3), "ms_total": ms,
+            "us_per_layer_call": ms * 1e3 / calls, "state_cache_gbs": 2 * state_bytes * calls / (ms * 1e-3) / 1e9,
+            "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_call": per_call, "launch": "CUDA graph per token"}
+
+
+# ---------------------------------------------------------------------------------------------
+# the reference arm: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    cfg = workloads.SCAN_CONFIGS[args.workload]
+    d = workloads.make_scan_inputs(cfg)
+    budget = 150.0  # seconds for the whole --steps K --warmup W run
+    rate0, nt, R0, secs0 = oracle_rate(d, 2.0)
+    per_step_s = min(5.0, budget / max(1, args.steps + args.warmup))
+    rows = max(1, int(rate0 * per_step_s / (cfg.seqlen * cfg.dstate)))
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(1)
+    R = cfg.batch * cfg.dim
+    sample = [(int(i // cfg.dim), int(i % cfg.dim)) for i in rng.choice(R, min(rows, R), replace=False)]
+    for _ in range(args.warmup):
+        oracle.scan(d, rows=sample)
+    t = time.time()
+    for _ in range(args.steps):
+        _, _, nt = oracle.scan(d, rows=sample)
+    secs = time.time() - t
+    elems = len(sample) * cfg.seqlen * cfg.dstate * args.steps
+    value = elems / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} "
+                                   f"L={cfg.seqlen}", "global_batch": cfg.batch, "seq_len": cfg.seqlen,
+                       "parallelism": "host threads over (b, d) rows"},
+            "cpu_baseline": {"value": value, "unit": "elem/s", "cores": nt, "kind": "oracle",
+                             "sample": f"{len(sample)} random (b, d) rows per step of {R}, full L={cfg.seqlen}"},
+            "e2e": {"value": value, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["b300", "reference"], default="b300")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.SCAN_CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch from an ncu capture of this kernel (reported as is)")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_b300(args, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

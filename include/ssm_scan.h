@@ -1,0 +1,159 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 selective state-space scan library (libssm_b300.so).
+ *
+ * The library computes the Mamba-1 selective scan, per batch row b, channel d and state n:
+ *
+ *   v_t   = u_t, or SiLU(conv_b[d] + sum_k conv_w[d,k] x_{t-W+1+k}) with the fused causal conv
+ *   dt_t  = softplus(delta_t + delta_bias[d])          (or delta_t + bias when softplus is off)
+ *   Abar  = exp(dt_t A[d,n])
+ *   Bbar  = (exp(dt_t A[d,n]) - 1) / A[d,n] * B_t[n]   zero-order hold (limit dt_t B_t[n] at A = 0)
+ *         = dt_t B_t[n]                                 simplified form
+ *   h_t[n] = Abar h_{t-1}[n] + Bbar v_t,  h_{-1} = h0 (or 0)
+ *   y_t   = (sum_n C_t[n] h_t[n] + Dskip[d] v_t) * SiLU(z_t)
+ *
+ * Sources (page address, section; two of the pages carry an unrelated site title):
+ *   zero-order hold and the recurrence: dpshk.com/news/3333417 sections 2.2, 2.3;
+ *     lshu.cn/news/79586 section 2.2;
+ *   diagonal (S4D) A, element-wise update: dpshk.com/news/3333417 section 3.2;
+ *   selection dt = softplus(.), input-dependent B and C: dpshk.com/news/3333417 section 4.1;
+ *     lshu.cn/news/79586 section 3.1 (B, C of shape (batch, seq_len, d_state));
+ *   simplified Bbar = dt B and the D skip: dpshk.com/news/3333417 section 5.1 (SelectiveSSM);
+ *   causal conv1d (padding W-1, cropped to L) + SiLU ahead of the SSM, gate y * SiLU(z):
+ *     dpshk.com/news/3333417 section 5.2 (MambaBlock); lshu.cn/news/79586 section 3.3;
+ *   carrying the final state of one segment into the next: pwwt.cn/news/5168881 section 3.1;
+ *   single-token step from a constant-size state cache: datadaily.news "State space models vs
+ *     Transformer: a practical guide", section on how state space models work; cache shape
+ *     (batch, d_inner, d_state): lshu.cn/news/79586 section 6.5.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers into memory the caller owns.  Every tensor is
+ *     dense row-major in the layout given below.  The library keeps no state between calls.
+ *     It allocates no memory: a call that needs scratch space takes a caller-provided workspace.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Errors: the return value is a status code.  Arguments are validated on the host before
+ *     anything is launched: no kernel runs on an invalid call.  ssm_last_error() returns a
+ *     thread-local message describing the most recent failure on the calling thread.  A launch
+ *     error reported by the CUDA runtime is returned as SSM_ERR_CUDA.  Faults inside a kernel
+ *     surface later, on the caller's next synchronisation, as with any CUDA launch.
+ *   - Any sequence length L >= 1 is accepted.  Unaligned base pointers or row lengths whose byte
+ *     size is not a multiple of 16 select a slower element-wise load path; they are not errors.
+ *   - Supported state sizes: 1 <= dstate <= 16, or dstate in {32, 64}.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *ssm_stream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,   /* null required pointer, non-positive size, bad enum value     */
+    SSM_ERR_UNSUPPORTED = 2,   /* well-formed request outside what the kernels implement       */
+    SSM_ERR_CUDA = 3           /* the CUDA runtime reported an error at launch                 */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/*
+ * Parameters of one selective scan.  Shapes: B = batch, D = dim (d_inner), N = dstate, L = seqlen.
+ *
+ *   u           (B, D, L) in_dtype   input v; the conv input x when conv_w != NULL      required
+ *   delta       (B, D, L) in_dtype   raw step before bias/softplus                       required
+ *   A           (D, N)    float32    diagonal state matrix (any finite value; 0 allowed)  required
+ *   Bm, Cm      (B, N, L) in_dtype   input-dependent B and C, shared by all D channels    required
+ *   Dskip       (D)       float32    skip weight, or NULL for none
+ *   delta_bias  (D)       float32    added to delta before softplus, or NULL for none
+ *   z           (B, D, L) in_dtype   gate input, or NULL for no gate
+ *   conv_w      (D, conv_width) f32  causal depthwise conv taps, or NULL for no conv;
+ *                                    tap conv_width-1 multiplies x_t
+ *   conv_b      (D)       float32    conv bias, or NULL for zero (ignored without conv_w)
+ *   conv_width  int                  1..4 when conv_w != NULL
+ *   h0          (B, D, N) float32    initial state, or NULL for zeros; may alias h_out
+ *   h_out       (B, D, N) float32    final state, or NULL if not wanted
+ *   y           (B, D, L) out_dtype  output; must not overlap any input
+ *   delta_softplus  1: dt = softplus(delta + bias); 0: dt = delta + bias
+ *   zoh             1: zero-order-hold Bbar;        0: simplified Bbar = dt B
+ *   workspace, workspace_bytes
+ *                   optional device scratch that lets the scan split L across thread blocks when
+ *                   B * D alone cannot fill the GPU.  NULL / too small is not an error: the call
+ *                   then runs without the split.  Size it with ssm_scan_workspace_size().  The
+ *                   workspace must not be shared by calls that may run concurrently.
+ */
+typedef struct ssm_scan_params {
+    int batch, dim, dstate, seqlen;
+    ssm_dtype in_dtype, out_dtype;
+    const void *u;
+    const void *delta;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *Dskip;
+    const float *delta_bias;
+    const void *z;
+    const float *conv_w;
+    const float *conv_b;
+    int conv_width;
+    const float *h0;
+    float *h_out;
+    void *y;
+    int delta_softplus;
+    int zoh;
+    void *workspace;
+    size_t workspace_bytes;
+} ssm_scan_params;
+
+/* Selective scan forward (with the optional fused conv front end, D skip and gate).
+   Errors: SSM_ERR_INVALID_ARG (null p, null required pointer, size <= 0, bad dtype/flag value,
+   conv_width outside 1..4), SSM_ERR_UNSUPPORTED (dstate not supported), SSM_ERR_CUDA. */
+SSM_API ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream);
+
+/* Bytes of workspace that let ssm_scan_fwd split L for this problem on the current device
+   (0 when no split would be used).  Returns 0 for an invalid p. */
+SSM_API size_t ssm_scan_workspace_size(const ssm_scan_params *p);
+
+/*
+ * Standalone causal depthwise conv1d (+ optional SiLU), the scan's front end on its own:
+ *   y[b,d,t] = act(b[d] + sum_{k<width} w[d,k] x[b,d,t-width+1+k]),  x before t = 0 is zero.
+ *   x, y (B, D, L) of `dtype`; w (D, width) float32; b (D) float32 or NULL.  width in 1..4.
+ *   y must not overlap x.
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_CUDA.
+ */
+SSM_API ssm_status causal_conv1d_fwd(const void *x, const float *w, const float *b, void *y, int batch, int dim,
+                             int seqlen, int width, int silu, ssm_dtype dtype, ssm_stream_t stream);
+
+/*
+ * Single-token decode step from a constant-size state cache (the scan body with L = 1):
+ *   state (B, D, N) float32, read and written in place
+ *   u, delta, z, y (B, D) of `dtype` (z may be NULL); Bm, Cm (B, N) of `dtype`
+ *   A (D, N) float32; Dskip, delta_bias (D) float32 or NULL
+ *   y must not overlap any input.
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED (dstate), SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *delta, const float *A, const void *Bm,
+                            const void *Cm, const float *Dskip, const float *delta_bias, const void *z, void *y,
+                            int batch, int dim, int dstate, int delta_softplus, int zoh, ssm_dtype dtype,
+                            ssm_stream_t stream);
+
+/* Thread-local description of the most recent failed call on this thread ("" if none). */
+SSM_API const char *ssm_last_error(void);
+
+/* Library version string. */
+SSM_API const char *ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

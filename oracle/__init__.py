@@ -84,8 +84,7 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
     Returns (y (R, L), h_out (R, N), threads_used) as fp64 numpy arrays.
     """
     lib = _load()
-    u = f64(inputs["u"])
-    Bsz, D, L = u.shape
+    Bsz, D, L = tuple(inputs["u"].shape)
     N = inputs["A"].shape[1]
     if rows is None:
         rb = np.repeat(np.arange(Bsz, dtype=np.int32), D)
@@ -96,12 +95,17 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
     R = len(rb)
 
     def rows_of(t, width):
-        a = f64(t)
-        if a is None:
+        if t is None:
             return None
         if rows is None:
-            return np.ascontiguousarray(a.reshape(R, width))
-        return np.ascontiguousarray(a[rb, rd])
+            return np.ascontiguousarray(f64(t).reshape(R, width))
+        # take the rows first, then widen: the full tensor is never converted
+        if hasattr(t, "detach"):
+            import torch
+            t = t.detach()[torch.as_tensor(rb, dtype=torch.long, device=t.device),
+                           torch.as_tensor(rd, dtype=torch.long, device=t.device)]
+            return np.ascontiguousarray(f64(t))
+        return np.ascontiguousarray(np.asarray(t, dtype=np.float64)[rb, rd])
 
     ur = rows_of(inputs["u"], L)
     dr = rows_of(inputs["delta"], L)
@@ -132,17 +136,20 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
 def conv1d(x, w, b=None, silu: bool = True, rows: Optional[Sequence[tuple]] = None):
     """Causal depthwise conv1d (+ optional SiLU) of x (B, D, L) with w (D, W), b (D,)."""
     lib = _load()
-    xa = f64(x)
-    Bsz, D, L = xa.shape
+    Bsz, D, L = tuple(x.shape)
     wa = f64(w)
     ba = f64(b)
     if rows is None:
         rd = np.tile(np.arange(D, dtype=np.int32), Bsz)
-        xr = np.ascontiguousarray(xa.reshape(Bsz * D, L))
+        xr = np.ascontiguousarray(f64(x).reshape(Bsz * D, L))
     else:
-        rb = np.asarray([r[0] for r in rows], dtype=np.int32)
+        rb = np.asarray([r[0] for r in rows], dtype=np.int64)
         rd = np.ascontiguousarray([r[1] for r in rows], dtype=np.int32)
-        xr = np.ascontiguousarray(xa[rb, rd])
+        if hasattr(x, "detach"):
+            import torch
+            xr = np.ascontiguousarray(f64(x.detach()[torch.as_tensor(rb), torch.as_tensor(rd, dtype=torch.long)]))
+        else:
+            xr = np.ascontiguousarray(np.asarray(x, dtype=np.float64)[rb, rd])
     R = len(rd)
     out = np.empty((R, L), dtype=np.float64)
     rc = lib.oracle_conv1d_rows(R, L, wa.shape[1], _iptr(rd), _ptr(xr), _ptr(wa), _ptr(ba), int(bool(silu)),

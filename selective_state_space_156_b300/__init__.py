@@ -1,0 +1,220 @@
+"""B300 (sm_103a) selective state-space scan: Python binding of libssm_b300.so.
+
+This module only marshals arguments: it checks that tensors live on the GPU with the expected
+dtype and layout, passes their device pointers and sizes to the C ABI (include/ssm_scan.h), and
+raises if a call fails.  Every step of the computation runs in the library's CUDA kernels.  There
+is no CPU fallback: importing works without the library, but any call raises if it is missing.
+
+Entry points (same names as the C ABI):
+  ssm_scan_fwd(u, delta, A, Bm, Cm, ...)      -> y  (and the final state if requested)
+  causal_conv1d_fwd(x, w, b=None, silu=True)  -> y
+  ssm_state_update(state, u, delta, A, Bm, Cm, ...)  -> y  (state updated in place)
+  ssm_scan_workspace_size(...)                -> bytes of optional scratch for the L split
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = ["ssm_scan_fwd", "causal_conv1d_fwd", "ssm_state_update", "ssm_scan_workspace_size", "lib",
+           "SsmError", "ScanParams", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssm_b300.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA = 0, 1, 2, 3
+SSM_F32, SSM_BF16 = 0, 1
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"[status {status}] {msg}")
+        self.status = status
+
+
+class ScanParams(ctypes.Structure):
+    """Mirror of ssm_scan_params in include/ssm_scan.h (same field order and types)."""
+    _fields_ = [
+        ("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int), ("seqlen", ctypes.c_int),
+        ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("A", ctypes.c_void_p),
+        ("Bm", ctypes.c_void_p), ("Cm", ctypes.c_void_p), ("Dskip", ctypes.c_void_p),
+        ("delta_bias", ctypes.c_void_p), ("z", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
+        ("conv_b", ctypes.c_void_p), ("conv_width", ctypes.c_int), ("h0", ctypes.c_void_p),
+        ("h_out", ctypes.c_void_p), ("y", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
+        ("zoh", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (ctypes).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m selective_state_space_156_b300.build`"
+                              " (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+        L.ssm_scan_fwd.restype = st
+        L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), vp]
+        L.ssm_scan_workspace_size.restype = ctypes.c_size_t
+        L.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+        L.causal_conv1d_fwd.restype = st
+        L.causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        L.ssm_state_update.restype = st
+        L.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        L.ssm_last_error.restype = ctypes.c_char_p
+        L.ssm_last_error.argtypes = []
+        L.ssm_version.restype = ctypes.c_char_p
+        L.ssm_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != SSM_OK:
+        raise SsmError(status, lib().ssm_last_error().decode())
+
+
+_DT = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, shape=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
+                 workspace) -> ScanParams:
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    Bsz, D, L = u.shape
+    N = A.shape[1]
+    idt = u.dtype
+    if idt not in _DT:
+        raise ValueError(f"unsupported input dtype {idt}")
+    p = ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen = Bsz, D, N, L
+    p.in_dtype = _DT[idt]
+    p.out_dtype = _DT[y.dtype] if y is not None else _DT[idt]
+    p.u = _ptr(u, "u", idt)
+    p.delta = _ptr(delta, "delta", idt, (Bsz, D, L))
+    p.A = _ptr(A, "A", torch.float32, (D, N))
+    p.Bm = _ptr(Bm, "Bm", idt, (Bsz, N, L))
+    p.Cm = _ptr(Cm, "Cm", idt, (Bsz, N, L))
+    p.Dskip = _ptr(Dskip, "Dskip", torch.float32, (D,))
+    p.delta_bias = _ptr(delta_bias, "delta_bias", torch.float32, (D,))
+    p.z = _ptr(z, "z", idt, (Bsz, D, L))
+    if conv_w is not None:
+        if conv_w.dim() != 2 or conv_w.shape[0] != D:
+            raise ValueError("conv_w must be (dim, width)")
+        p.conv_w = _ptr(conv_w, "conv_w", torch.float32)
+        p.conv_width = conv_w.shape[1]
+        p.conv_b = _ptr(conv_b, "conv_b", torch.float32, (D,))
+    p.h0 = _ptr(h0, "h0", torch.float32, (Bsz, D, N))
+    p.h_out = _ptr(h_out, "h_out", torch.float32, (Bsz, D, N))
+    p.y = _ptr(y, "y", None, (Bsz, D, L)) if y is not None else None
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    if workspace is not None:
+        p.workspace = _ptr(workspace, "workspace", torch.uint8)
+        p.workspace_bytes = workspace.numel()
+    return p
+
+
+def ssm_scan_workspace_size(u, delta, A, Bm, Cm, **kw) -> int:
+    """Bytes of scratch that let ssm_scan_fwd split L for this problem (0 = no split needed)."""
+    y = kw.pop("y", None)
+    if y is None:
+        y = torch.empty_like(u, dtype=kw.pop("out_dtype", None) or u.dtype)
+    p = _scan_params(u, delta, A, Bm, Cm, kw.get("Dskip"), kw.get("delta_bias"), kw.get("z"), kw.get("conv_w"),
+                     kw.get("conv_b"), kw.get("h0"), kw.get("h_out"), y, kw.get("delta_softplus", True),
+                     kw.get("zoh", True), None)
+    return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
+
+
+def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
+                 Dskip: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                 z: Optional[torch.Tensor] = None, conv_w: Optional[torch.Tensor] = None,
+                 conv_b: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
+                 h_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                 delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
+                 workspace: Optional[torch.Tensor] = None, return_state: bool = False, stream=None):
+    """Selective scan forward on the GPU.  Layouts as in include/ssm_scan.h: u/delta/z/y (B, D, L),
+    Bm/Cm (B, N, L), A (D, N) fp32, Dskip/delta_bias/conv_b (D,) fp32, conv_w (D, W) fp32,
+    h0/h_out (B, D, N) fp32.  ``workspace`` (uint8 CUDA tensor, optional) enables the L split;
+    pass ``workspace="auto"`` to allocate it here.  Returns y, or (y, h_out) with return_state."""
+    if y is None:
+        y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
+    if return_state and h_out is None:
+        h_out = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+    if isinstance(workspace, str) and workspace == "auto":
+        n = ssm_scan_workspace_size(u, delta, A, Bm, Cm, Dskip=Dskip, delta_bias=delta_bias, z=z, conv_w=conv_w,
+                                    conv_b=conv_b, h0=h0, h_out=h_out, y=y, delta_softplus=delta_softplus, zoh=zoh)
+        workspace = torch.empty(n, dtype=torch.uint8, device=u.device) if n > 0 else None
+    p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
+                     workspace)
+    _check(lib().ssm_scan_fwd(ctypes.byref(p), _stream(stream)))
+    return (y, h_out) if return_state else y
+
+
+def causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, b: Optional[torch.Tensor] = None, silu: bool = True,
+                      y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal depthwise conv1d (+ SiLU) of x (B, D, L) with taps w (D, W) fp32 and bias b (D,) fp32."""
+    if x.dim() != 3:
+        raise ValueError("x must be (batch, dim, seqlen)")
+    Bsz, D, L = x.shape
+    if x.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    if y is None:
+        y = torch.empty_like(x)
+    if w.dim() != 2 or w.shape[0] != D:
+        raise ValueError("w must be (dim, width)")
+    _check(lib().causal_conv1d_fwd(_ptr(x, "x"), _ptr(w, "w", torch.float32), _ptr(b, "b", torch.float32, (D,)),
+                                   _ptr(y, "y", x.dtype, (Bsz, D, L)), Bsz, D, L, w.shape[1], int(bool(silu)),
+                                   _DT[x.dtype], _stream(stream)))
+    return y
+
+
+def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor,
+                     Cm: torch.Tensor, Dskip: Optional[torch.Tensor] = None,
+                     delta_bias: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                     y: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = True,
+                     stream=None) -> torch.Tensor:
+    """One decode step: state (B, D, N) fp32 updated in place; u/delta/z (B, D), Bm/Cm (B, N).  Returns y (B, D)."""
+    Bsz, D, N = state.shape
+    dt = u.dtype
+    if dt not in _DT:
+        raise ValueError(f"unsupported dtype {dt}")
+    if y is None:
+        y = torch.empty_like(u)
+    _check(lib().ssm_state_update(_ptr(state, "state", torch.float32), _ptr(u, "u", dt, (Bsz, D)),
+                                  _ptr(delta, "delta", dt, (Bsz, D)), _ptr(A, "A", torch.float32, (D, N)),
+                                  _ptr(Bm, "Bm", dt, (Bsz, N)), _ptr(Cm, "Cm", dt, (Bsz, N)),
+                                  _ptr(Dskip, "Dskip", torch.float32, (D,)),
+                                  _ptr(delta_bias, "delta_bias", torch.float32, (D,)), _ptr(z, "z", dt, (Bsz, D)),
+                                  _ptr(y, "y", dt, (Bsz, D)), Bsz, D, N, int(bool(delta_softplus)), int(bool(zoh)),
+                                  _DT[dt], _stream(stream)))
+    return y

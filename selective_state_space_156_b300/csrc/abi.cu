@@ -1,0 +1,206 @@
+// extern "C" entry points of libssm_b300.so: argument validation, launch-shape choice and dispatch.
+// Declarations, argument meaning, layouts, ownership and error behaviour: include/ssm_scan.h.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "ssm_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ssm_status fail(ssm_status code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+ssm_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return SSM_OK;
+    return fail(SSM_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+size_t esize(int dtype) { return dtype == SSM_BF16 ? 2 : 4; }
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    if (a == nullptr || b == nullptr) return false;
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+// Segmenting of L.  One segment unless the (b, channel-block) grid fills under half of the GPU's
+// resident block slots; then L is cut into enough segments of at least 512 steps to fill it.
+struct SegPlan {
+    int nseg;
+    int seg_len;
+};
+
+SegPlan plan_segments(int Bsz, int D, int L) {
+    const long long blocks = (long long)((D + ssm::kScanThreads - 1) / ssm::kScanThreads) * Bsz;
+    const long long slots = (long long)sm_count() * 3;  // resident 128-thread scan blocks per SM
+    SegPlan p{1, ((L + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk};
+    if (blocks * 2 >= slots) return p;
+    long long want = (slots + blocks - 1) / blocks;
+    long long maxseg = L / 512;
+    if (want > maxseg) want = maxseg;
+    if (want > 64) want = 64;
+    if (want <= 1) return p;
+    int seg = (int)(((L + want - 1) / want + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk;
+    p.seg_len = seg;
+    p.nseg = (L + seg - 1) / seg;
+    return p;
+}
+
+size_t workspace_bytes_for(const ssm_scan_params* p, const SegPlan& sp) {
+    if (sp.nseg <= 1) return 0;
+    const size_t rows = (size_t)p->batch * p->dim;
+    size_t bytes = (size_t)(sp.nseg - 1) * rows * ((size_t)p->dstate + 1) * sizeof(float);
+    if (p->h0 != nullptr) bytes += rows * (size_t)p->dstate * sizeof(float);
+    return bytes + 256;
+}
+
+bool dstate_supported(int n) { return n >= 1 && n <= 16; }
+
+ssm_status validate_scan(const ssm_scan_params* p) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: params is NULL");
+    if (p->batch <= 0 || p->dim <= 0 || p->dstate <= 0 || p->seqlen <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: sizes must be positive (batch=%d dim=%d dstate=%d seqlen=%d)",
+                    p->batch, p->dim, p->dstate, p->seqlen);
+    if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: batch %d exceeds 65535", p->batch);
+    if ((p->in_dtype != SSM_F32 && p->in_dtype != SSM_BF16) || (p->out_dtype != SSM_F32 && p->out_dtype != SSM_BF16))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: bad dtype (in=%d out=%d)", (int)p->in_dtype, (int)p->out_dtype);
+    if (!p->u || !p->delta || !p->A || !p->Bm || !p->Cm || !p->y)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: u, delta, A, Bm, Cm and y are required");
+    if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->zoh != 0 && p->zoh != 1))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: delta_softplus and zoh must be 0 or 1");
+    if (p->conv_w != nullptr && (p->conv_width < 1 || p->conv_width > 4))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: conv_width %d outside 1..4", p->conv_width);
+    if (!dstate_supported(p->dstate))
+        return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: dstate %d not supported (1..16)", p->dstate);
+    const size_t rows = (size_t)p->batch * p->dim;
+    if (rows * (size_t)p->seqlen >= ((size_t)1 << 40))
+        return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: batch*dim*seqlen too large");
+    const size_t ib = esize(p->in_dtype), ob = esize(p->out_dtype);
+    const size_t nbdl = rows * (size_t)p->seqlen;
+    const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
+    const size_t ybytes = nbdl * ob;
+    if (overlaps(p->y, ybytes, p->u, nbdl * ib) || overlaps(p->y, ybytes, p->delta, nbdl * ib) ||
+        overlaps(p->y, ybytes, p->z, nbdl * ib) || overlaps(p->y, ybytes, p->Bm, nbnl * ib) ||
+        overlaps(p->y, ybytes, p->Cm, nbnl * ib))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: y overlaps an input");
+    if (p->h_out != nullptr && overlaps(p->h_out, rows * p->dstate * 4, p->y, ybytes))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_out overlaps y");
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_last_error(void) { return g_last_error.c_str(); }
+
+const char* ssm_version(void) { return "ssm_b300 0.1 (sm_103a)"; }
+
+size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
+    if (validate_scan(p) != SSM_OK) return 0;
+    return workspace_bytes_for(p, plan_segments(p->batch, p->dim, p->seqlen));
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
+    ssm_status st = validate_scan(p);
+    if (st != SSM_OK) return st;
+
+    ssm::ScanKernelArgs a{};
+    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
+    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm;
+    a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
+    a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
+    a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
+    a.softplus = p->delta_softplus;
+    const size_t ib = esize(p->in_dtype), ob = esize(p->out_dtype);
+    a.vec = ((size_t)p->seqlen % 8 == 0) && aligned16(p->u) && aligned16(p->delta) && aligned16(p->y) &&
+            (p->z == nullptr || aligned16(p->z)) && ib * 8 % 16 == 0 && ob * 8 % 16 == 0;
+
+    SegPlan sp = plan_segments(p->batch, p->dim, p->seqlen);
+    const size_t need = workspace_bytes_for(p, sp);
+    if (sp.nseg > 1 && (p->workspace == nullptr || p->workspace_bytes < need))
+        sp = SegPlan{1, ((p->seqlen + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk};
+    a.nseg = sp.nseg;
+    a.seg_len = sp.seg_len;
+    if (sp.nseg > 1) {
+        uintptr_t base = (reinterpret_cast<uintptr_t>(p->workspace) + 255) & ~(uintptr_t)255;
+        const size_t rows = (size_t)p->batch * p->dim;
+        float* w = reinterpret_cast<float*>(base);
+        a.ws_dsum = w;
+        a.ws_h = w + (size_t)(sp.nseg - 1) * rows;
+        a.ws_h0 = p->h0 != nullptr ? a.ws_h + (size_t)(sp.nseg - 1) * rows * p->dstate : nullptr;
+    }
+    return cuda_status(ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream),
+                       "ssm_scan_fwd launch");
+}
+
+ssm_status causal_conv1d_fwd(const void* x, const float* w, const float* b, void* y, int batch, int dim, int seqlen,
+                             int width, int silu, ssm_dtype dtype, ssm_stream_t stream) {
+    if (!x || !w || !y) return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: x, w and y are required");
+    if (batch <= 0 || dim <= 0 || seqlen <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: sizes must be positive");
+    if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "causal_conv1d_fwd: batch %d exceeds 65535", batch);
+    if (width < 1 || width > 4) return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: width %d outside 1..4", width);
+    if (silu != 0 && silu != 1) return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: silu must be 0 or 1");
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: bad dtype");
+    const size_t bytes = (size_t)batch * dim * seqlen * esize(dtype);
+    if (overlaps(x, bytes, y, bytes)) return fail(SSM_ERR_INVALID_ARG, "causal_conv1d_fwd: y overlaps x");
+    return cuda_status(ssm::launch_causal_conv1d(x, w, b, y, batch, dim, seqlen, width, silu, (int)dtype,
+                                                 (cudaStream_t)stream),
+                       "causal_conv1d_fwd launch");
+}
+
+ssm_status ssm_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                            const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
+                            int batch, int dim, int dstate, int delta_softplus, int zoh, ssm_dtype dtype,
+                            ssm_stream_t stream) {
+    if (!state || !u || !delta || !A || !Bm || !Cm || !y)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: state, u, delta, A, Bm, Cm and y are required");
+    if (batch <= 0 || dim <= 0 || dstate <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: sizes must be positive");
+    if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "ssm_state_update: batch %d exceeds 65535", batch);
+    if (!(dstate <= 16 || dstate == 32 || dstate == 64))
+        return fail(SSM_ERR_UNSUPPORTED, "ssm_state_update: dstate %d not supported (1..16, 32, 64)", dstate);
+    if ((delta_softplus != 0 && delta_softplus != 1) || (zoh != 0 && zoh != 1))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: delta_softplus and zoh must be 0 or 1");
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: bad dtype");
+    const size_t bd = (size_t)batch * dim * esize(dtype);
+    const size_t bn = (size_t)batch * dstate * esize(dtype);
+    if (overlaps(y, bd, u, bd) || overlaps(y, bd, delta, bd) || overlaps(y, bd, z, bd) || overlaps(y, bd, Bm, bn) ||
+        overlaps(y, bd, Cm, bn) || overlaps(y, bd, state, (size_t)batch * dim * dstate * 4))
+        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: y overlaps an input or the state");
+    return cuda_status(ssm::launch_state_update(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, batch, dim, dstate,
+                                                delta_softplus, zoh, (int)dtype, (cudaStream_t)stream),
+                       "ssm_state_update launch");
+}
+
+}  // extern "C"
+
+namespace ssm {
+cudaError_t launch_scan(const ScanKernelArgs& a, int in_dtype, int out_dtype, int zoh, cudaStream_t stream) {
+    if (in_dtype == 0 && out_dtype == 0) return launch_scan_f32_f32(a, zoh, stream);
+    if (in_dtype == 1 && out_dtype == 1) return launch_scan_bf16_bf16(a, zoh, stream);
+    if (in_dtype == 1 && out_dtype == 0) return launch_scan_bf16_f32(a, zoh, stream);
+    return launch_scan_f32_bf16(a, zoh, stream);
+}
+}  // namespace ssm

@@ -1,0 +1,78 @@
+// Standalone causal depthwise conv1d (+ optional SiLU): the front end of the Mamba block
+// (dpshk.com/news/3333417 section 5.2: Conv1d with padding width-1, groups = channels, output
+// cropped to the first L steps, then SiLU).  Tap k of a width-W filter multiplies x_{t-W+1+k}.
+// HBM-bound: one read of x and one write of y.
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+constexpr int kConvThreads = 128;
+constexpr int kConvTile = 512;  // timesteps per thread
+
+template <typename T>
+__global__ void __launch_bounds__(kConvThreads) causal_conv1d_kernel(const void* __restrict__ x, const float* __restrict__ w,
+                                                                     const float* __restrict__ bias, void* __restrict__ y,
+                                                                     int D, int L, int W, int silu_on, int vec) {
+    const int d = blockIdx.x * kConvThreads + threadIdx.x;
+    if (d >= D) return;
+    const size_t row = (size_t)blockIdx.y * D + d;
+    const size_t rowoff = row * (size_t)L;
+    const int t0 = blockIdx.z * kConvTile;
+    const int t1 = min(L, t0 + kConvTile);
+
+    float wk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int k = 0; k < W; ++k) wk[4 - W + k] = __ldg(w + (size_t)d * W + k);
+    const float cb = bias != nullptr ? __ldg(bias + d) : 0.0f;
+    float xh[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int t = t0 - 3 + k;
+        xh[k] = t >= 0 ? load1<T>(x, rowoff + t) : 0.0f;
+    }
+
+    for (int tg = t0; tg < t1; tg += 8) {
+        const int nv = min(8, t1 - tg);
+        float xv[8], out[8];
+        if (vec && nv == 8) {
+            load8<T>(x, rowoff + tg, xv);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xv[j] = j < nv ? load1<T>(x, rowoff + tg + j) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float acc = fmaf(wk[0], xh[0], cb);
+            acc = fmaf(wk[1], xh[1], acc);
+            acc = fmaf(wk[2], xh[2], acc);
+            acc = fmaf(wk[3], xv[j], acc);
+            xh[0] = xh[1];
+            xh[1] = xh[2];
+            xh[2] = xv[j];
+            out[j] = silu_on ? silu(acc) : acc;
+        }
+        if (vec && nv == 8) {
+            store8<T>(y, rowoff + tg, out);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < nv) store1<T>(y, rowoff + tg + j, out[j]);
+        }
+    }
+}
+
+cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, void* y, int Bsz, int D, int L, int width,
+                                 int silu_on, int dtype, cudaStream_t stream) {
+    const int esize = dtype == 1 ? 2 : 4;
+    const int vec = (((size_t)L * esize) % 16 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(y) & 15) == 0);
+    dim3 block(kConvThreads);
+    dim3 grid((unsigned)((D + kConvThreads - 1) / kConvThreads), (unsigned)Bsz, (unsigned)((L + kConvTile - 1) / kConvTile));
+    if (dtype == 1)
+        causal_conv1d_kernel<BF16><<<grid, block, 0, stream>>>(x, w, b, y, D, L, width, silu_on, vec);
+    else
+        causal_conv1d_kernel<F32><<<grid, block, 0, stream>>>(x, w, b, y, D, L, width, silu_on, vec);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -1,0 +1,58 @@
+// Host-side declarations shared by the translation units of libssm_b300.so.
+#pragma once
+
+#include <cstddef>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ssm_scan.h"
+
+namespace ssm {
+
+// Everything a scan launch needs, after host-side validation.
+struct ScanKernelArgs {
+    int Bsz, D, N, L;
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* Bm;
+    const void* Cm;
+    const float* Dskip;
+    const float* delta_bias;
+    const void* z;
+    const float* conv_w;
+    const float* conv_b;
+    int conv_width;
+    const float* h0;
+    float* h_out;
+    void* y;
+    int softplus;
+    int vec;       // 1: every (b, d) row of u/delta/z/y starts 16-byte aligned and L % 8 == 0
+    int nseg;      // number of L segments (1 = one pass, no workspace)
+    int seg_len;   // timesteps per segment, a multiple of the chunk length; last one may be shorter
+    float* ws_h;     // (nseg - 1, B*D, N) end state of each segment but the last, from a zero start
+    float* ws_dsum;  // (nseg - 1, B*D) sum of dt over each segment but the last
+    float* ws_h0;    // (B*D, N) copy of h0 taken before any block may write h_out (h0 may alias h_out)
+};
+
+constexpr int kScanThreads = 128;  // channels per block in the scan kernels
+constexpr int kScanChunk = 64;     // timesteps of B/C staged in shared memory at a time
+
+// Launches the summary (when nseg > 1) and final scan kernels.  in/out: 0 = f32, 1 = bf16.
+cudaError_t launch_scan(const ScanKernelArgs& a, int in_dtype, int out_dtype, int zoh, cudaStream_t stream);
+
+cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, void* y, int Bsz, int D, int L,
+                                 int width, int silu, int dtype, cudaStream_t stream);
+
+cudaError_t launch_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
+                                int Bsz, int D, int N, int softplus, int zoh, int dtype, cudaStream_t stream);
+
+// Per-dtype-combination entry points defined in scan_<in>_<out>.cu.
+cudaError_t launch_scan_f32_f32(const ScanKernelArgs& a, int zoh, cudaStream_t s);
+cudaError_t launch_scan_bf16_bf16(const ScanKernelArgs& a, int zoh, cudaStream_t s);
+cudaError_t launch_scan_bf16_f32(const ScanKernelArgs& a, int zoh, cudaStream_t s);
+cudaError_t launch_scan_f32_bf16(const ScanKernelArgs& a, int zoh, cudaStream_t s);
+
+}  // namespace ssm
