@@ -307,7 +307,7 @@ def run_b300(args, rank, world, local):
     hbm_peak = peaks.get("hbm_gbs")
     hbm_src = "measured" if hbm_peak else "fallback"
     hbm_peak = hbm_peak or FALLBACK_HBM_GBS
-    rate_clk, probe = mufu_rate_per_clk(True) if rank == 0 else (32.0, {})
+    rate_clk, probe = mufu_rate_per_clk(not args.no_peaks) if rank == 0 else (32.0, {})
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mufu_peak = sms * rate_clk * MAX_SM_MHZ * 1e6           # ex2-class ops / s
     mufu_ops = scan_mufu_ops(cfg)
@@ -452,6 +452,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-peaks", action="store_true", help="skip the bench_peaks.cu MUFU-rate probe")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

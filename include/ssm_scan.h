@@ -37,7 +37,9 @@
  *     surface later, on the caller's next synchronisation, as with any CUDA launch.
  *   - Any sequence length L >= 1 is accepted.  Unaligned base pointers or row lengths whose byte
  *     size is not a multiple of 16 select a slower element-wise load path; they are not errors.
- *   - Supported state sizes: 1 <= dstate <= 16, or dstate in {32, 64}.
+ *   - Supported state sizes: 1 <= dstate <= 16 for every dtype; 32 and 64 for bf16 inputs and
+ *     output with 16-byte-aligned rows and seqlen % 8 == 0 (ssm_scan_fwd); any of 1..16, 32, 64
+ *     for ssm_state_update.
  */
 #ifndef SSM_SCAN_H
 #define SSM_SCAN_H

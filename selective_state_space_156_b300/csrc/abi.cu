@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 
 #include "ssm_internal.h"
@@ -43,24 +44,69 @@ int sm_count() {
     return n;
 }
 
-// Segmenting of L.  One segment unless the (b, channel-block) grid fills under half of the GPU's
-// resident block slots; then L is cut into enough segments of at least 512 steps to fill it.
+// Which kernel runs a problem: the four-lanes-per-channel kernel for aligned bf16-in/bf16-out
+// problems (its tensor-core readout rounds h to tf32, fine for a bf16 result), the one-row-per-thread
+// kernel otherwise.
+bool aligned_rows(const ssm_scan_params* p) {
+    const size_t ib = esize(p->in_dtype), ob = esize(p->out_dtype);
+    return ((size_t)p->seqlen % 8 == 0) && aligned16(p->u) && aligned16(p->delta) && aligned16(p->y) &&
+           (p->z == nullptr || aligned16(p->z)) && aligned16(p->Bm) && aligned16(p->Cm) && ib * 8 % 16 == 0 &&
+           ob * 8 % 16 == 0;
+}
+
+int scan_kind(const ssm_scan_params* p) {
+    if (p->in_dtype == SSM_BF16 && p->out_dtype == SSM_BF16 && aligned_rows(p)) {
+        if (p->dstate <= 16) return ssm::kScanP16;
+        if (p->dstate <= 64) return ssm::kScanG4;
+    }
+    return ssm::kScanSeq;
+}
+
+struct KindGeom {
+    int chan_per_block, blocks_per_sm, chunk;
+};
+
+// Resident blocks per SM of the packed kernel by lanes per channel (its launch bounds).
+int p16_blocks_per_sm(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
+
+KindGeom kind_geom(int kind, int lpc) {
+    if (kind == ssm::kScanG4) return {ssm::kG4ChanPerBlock, ssm::kG4BlocksPerSM, ssm::kG4ChunkSteps};
+    if (kind == ssm::kScanP16) return {ssm::kP16Threads_ / lpc, p16_blocks_per_sm(lpc), ssm::kP16ChunkSteps};
+    return {ssm::kSeqChanPerBlock, ssm::kSeqBlocksPerSM, ssm::kSeqChunk};
+}
+
+// Lanes per channel of the packed kernel.  More lanes per channel give more warps (better latency
+// hiding) at a higher per-step cost; SSM_SCAN_LANES_PER_CHANNEL (1, 2 or 4) overrides the choice.
+int choose_lpc(const ssm_scan_params* p) {
+    if (const char* env = getenv("SSM_SCAN_LANES_PER_CHANNEL")) {
+        const int v = atoi(env);
+        if (v == 1 || v == 2 || v == 4) return p->dstate <= 4 ? 1 : (p->dstate <= 8 && v > 2 ? 2 : v);
+    }
+    (void)p;
+    return 1;  // measured fastest on the 8 x 4096 x 16 x 2048 and 1 x 5120 x 16 x 65536 workloads
+}
+
+// Segmenting of L.  One segment while the (b, channel-block) grid fills at least half of the GPU's
+// resident block slots; otherwise L is cut into as many segments (each >= 512 steps) as still fit in
+// one round of resident blocks, so the final pass never needs a second wave.
 struct SegPlan {
     int nseg;
     int seg_len;
 };
 
-SegPlan plan_segments(int Bsz, int D, int L) {
-    const long long blocks = (long long)((D + ssm::kScanThreads - 1) / ssm::kScanThreads) * Bsz;
-    const long long slots = (long long)sm_count() * 3;  // resident 128-thread scan blocks per SM
-    SegPlan p{1, ((L + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk};
+SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
+    const KindGeom kg = kind_geom(kind, lpc);
+    const int cpb = kg.chan_per_block, bps = kg.blocks_per_sm, chunk = kg.chunk;
+    const long long blocks = (long long)((D + cpb - 1) / cpb) * Bsz;
+    const long long slots = (long long)sm_count() * bps;
+    SegPlan p{1, ((L + chunk - 1) / chunk) * chunk};
     if (blocks * 2 >= slots) return p;
-    long long want = (slots + blocks - 1) / blocks;
-    long long maxseg = L / 512;
+    long long want = slots / blocks;
+    const long long maxseg = L / 512;
     if (want > maxseg) want = maxseg;
     if (want > 64) want = 64;
     if (want <= 1) return p;
-    int seg = (int)(((L + want - 1) / want + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk;
+    const int seg = (int)(((L + want - 1) / want + chunk - 1) / chunk) * chunk;
     p.seg_len = seg;
     p.nseg = (L + seg - 1) / seg;
     return p;
@@ -74,7 +120,10 @@ size_t workspace_bytes_for(const ssm_scan_params* p, const SegPlan& sp) {
     return bytes + 256;
 }
 
-bool dstate_supported(int n) { return n >= 1 && n <= 16; }
+bool dstate_supported(const ssm_scan_params* p) {
+    if (p->dstate >= 1 && p->dstate <= 16) return true;
+    return (p->dstate == 32 || p->dstate == 64) && scan_kind(p) == ssm::kScanG4;
+}
 
 ssm_status validate_scan(const ssm_scan_params* p) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: params is NULL");
@@ -90,8 +139,10 @@ ssm_status validate_scan(const ssm_scan_params* p) {
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: delta_softplus and zoh must be 0 or 1");
     if (p->conv_w != nullptr && (p->conv_width < 1 || p->conv_width > 4))
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: conv_width %d outside 1..4", p->conv_width);
-    if (!dstate_supported(p->dstate))
-        return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: dstate %d not supported (1..16)", p->dstate);
+    if (!dstate_supported(p))
+        return fail(SSM_ERR_UNSUPPORTED,
+                    "ssm_scan_fwd: dstate %d not supported (1..16; 32 and 64 need bf16 in/out, 16-byte-aligned "
+                    "rows and seqlen %% 8 == 0)", p->dstate);
     const size_t rows = (size_t)p->batch * p->dim;
     if (rows * (size_t)p->seqlen >= ((size_t)1 << 40))
         return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: batch*dim*seqlen too large");
@@ -118,7 +169,7 @@ const char* ssm_version(void) { return "ssm_b300 0.1 (sm_103a)"; }
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     if (validate_scan(p) != SSM_OK) return 0;
-    return workspace_bytes_for(p, plan_segments(p->batch, p->dim, p->seqlen));
+    return workspace_bytes_for(p, plan_segments(scan_kind(p), choose_lpc(p), p->batch, p->dim, p->seqlen));
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
@@ -132,14 +183,16 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
     a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
     a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
     a.softplus = p->delta_softplus;
-    const size_t ib = esize(p->in_dtype), ob = esize(p->out_dtype);
-    a.vec = ((size_t)p->seqlen % 8 == 0) && aligned16(p->u) && aligned16(p->delta) && aligned16(p->y) &&
-            (p->z == nullptr || aligned16(p->z)) && ib * 8 % 16 == 0 && ob * 8 % 16 == 0;
+    a.vec = aligned_rows(p);
+    a.kind = scan_kind(p);
+    a.lpc = choose_lpc(p);
 
-    SegPlan sp = plan_segments(p->batch, p->dim, p->seqlen);
+    SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
     const size_t need = workspace_bytes_for(p, sp);
-    if (sp.nseg > 1 && (p->workspace == nullptr || p->workspace_bytes < need))
-        sp = SegPlan{1, ((p->seqlen + ssm::kScanChunk - 1) / ssm::kScanChunk) * ssm::kScanChunk};
+    if (sp.nseg > 1 && (p->workspace == nullptr || p->workspace_bytes < need)) {
+        const int chunk = kind_geom(a.kind, a.lpc).chunk;
+        sp = SegPlan{1, ((p->seqlen + chunk - 1) / chunk) * chunk};
+    }
     a.nseg = sp.nseg;
     a.seg_len = sp.seg_len;
     if (sp.nseg > 1) {

@@ -22,7 +22,9 @@ __global__ void __launch_bounds__(kConvThreads) causal_conv1d_kernel(const void*
     const int t1 = min(L, t0 + kConvTile);
 
     float wk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int k = 0; k < W; ++k) wk[4 - W + k] = __ldg(w + (size_t)d * W + k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)  // tap i of the 4-wide window is tap i - (4 - W) of the filter
+        wk[i] = i >= 4 - W ? __ldg(w + (size_t)d * W + i - (4 - W)) : 0.0f;
     const float cb = bias != nullptr ? __ldg(bias + d) : 0.0f;
     float xh[3];
 #pragma unroll

@@ -24,8 +24,6 @@
 
 namespace ssm {
 
-enum class Disc { kZOH, kZOHSafe, kSimple };
-
 template <int NS>
 struct ScanShared {
     float bc[2][kScanChunk][NS];  // [0] = B_t[n], [1] = C_t[n], fp32, zero past L and past N
@@ -204,7 +202,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
     cc.cb = 0.0f;
     if (a.conv_w != nullptr && active) {
         const int W = a.conv_width;
-        for (int k = 0; k < W; ++k) cc.w[4 - W + k] = __ldg(a.conv_w + (size_t)d * W + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)  // tap i of the 4-wide window is tap i - (4 - W) of the filter
+            cc.w[i] = i >= 4 - W ? __ldg(a.conv_w + (size_t)d * W + i - (4 - W)) : 0.0f;
         if (a.conv_b != nullptr) cc.cb = __ldg(a.conv_b + d);
     }
     cc.dskip = (a.Dskip != nullptr && active) ? __ldg(a.Dskip + d) : 0.0f;

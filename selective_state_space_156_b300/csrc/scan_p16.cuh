@@ -1,0 +1,407 @@
+// Selective-scan kernel for aligned bf16 problems: LPC lanes per channel, packed fp32 pairs.
+//
+// Layout.  A block of 128 threads owns 128 / LPC channels of one batch row and one L segment.  The
+// LPC lanes of a channel each keep N / LPC of its fp32 states in registers and walk the segment in
+// time order, so the recurrence h_t = Abar h_{t-1} + Bbar v_t (dpshk.com/news/3333417 sections
+// 2.2/2.3; the diagonal A of section 3.2 decouples the states) needs no exchange between lanes; only
+// the readout y = sum_n C h is summed over the LPC lanes with xor shuffles.  LPC trades per-step
+// overhead (shared by N / LPC states per lane) against warps per SM (latency hiding): the host picks it
+// from the problem size.  The state update and the readout run on pairs of states with the sm_100+
+// packed f32x2 instructions: one issue slot per two lanes of FMA work.
+//
+// Per-step scalars.  Within a group of 8 steps, lane e of a channel computes the conv front end,
+// softplus and gate of steps [e 8/LPC, (e+1) 8/LPC); the (dt, v) of the other steps come from the
+// owning lanes by shuffle, and each lane applies the D skip and gate to, and stores, its own steps.
+//
+// Zero-order hold per state pair, with ninv = -1/a and ng = (v ninv) B = -(v/a) B:
+//   h' = Abar (h - ng) + ng  ==  Abar h + (Abar - 1)(v/a) B,
+// whose fixed point for a constant input is -ng exactly, whatever the rounding of Abar.  A block in
+// which some a == 0 runs a second loop body that uses the a -> 0 limit dt B (lshu.cn/news/79586 2.2).
+//
+// Staging.  Per 32-step chunk, cp.async copies the block's u/x rows (with an 8-step halo for the conv
+// front end of dpshk.com/news/3333417 section 5.2), delta and z rows and the B/C rows of the batch row
+// into shared memory one chunk ahead (double buffer); B/C are widened to fp32 once per chunk and read
+// by every lane as broadcasts.  Outputs leave as 16-byte stores of 8 steps.  Requires L % 8 == 0 and
+// 16-byte-aligned rows (the host checks).  bf16 outputs use MUFU tanh/lg2 forms of SiLU and softplus.
+#pragma once
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+constexpr int kP16Threads = 128;              // threads per block
+constexpr int kP16Chunk = 32;                 // steps per staged chunk
+constexpr int kP16Halo = 8;                   // x steps staged before the chunk (conv history)
+constexpr int kP16Row = kP16Halo + kP16Chunk; // staged row length in elements (80 B)
+constexpr int kP16Segs = kP16Chunk / 8;       // 16-byte segments per staged row
+
+template <int NS, int LPC>
+struct P16Smem {
+    static constexpr int kCh = kP16Threads / LPC;  // channels per block
+    uint16_t x[2][kCh][kP16Row];               // bf16 u / x, steps c0-8 .. c0+31
+    uint16_t dl[2][kCh][kP16Row];              // bf16 delta at [8 + t - c0]
+    uint16_t zz[2][kCh][kP16Row];              // bf16 z at [8 + t - c0]
+    uint16_t bcr[2][2][NS][kP16Row];           // raw bf16 B / C rows (n, t), padded against bank conflicts
+    float bc[kP16Chunk][2][NS];                // fp32 B_t[n], C_t[n]
+};
+
+__device__ __forceinline__ void p16_cp_async16(void* smem, const void* gmem, bool valid) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int n = valid ? 16 : 0;  // 0: fill the 16 bytes with zeros, read nothing
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+
+template <int NS, int LPC>
+__device__ __forceinline__ void p16_issue_chunk(const ScanKernelArgs& a, P16Smem<NS, LPC>& sm, int buf, int b, int ch0,
+                                                int c0, bool want_z) {
+    constexpr int kCh = P16Smem<NS, LPC>::kCh;
+    const int tid = threadIdx.x;
+    const uint16_t* u = static_cast<const uint16_t*>(a.u);
+    const uint16_t* dl = static_cast<const uint16_t*>(a.delta);
+    const uint16_t* zz = static_cast<const uint16_t*>(a.z);
+    const bool conv = a.conv_w != nullptr;
+    // rows of u / x: the halo segment only when the conv needs it
+    for (int i = tid; i < kCh * (kP16Segs + 1); i += kP16Threads) {
+        const int r = i / (kP16Segs + 1), s = i - r * (kP16Segs + 1);
+        if (s == 0 && !conv) continue;
+        const int d = ch0 + r;
+        const int t = c0 - kP16Halo + 8 * s;
+        const bool ok = d < a.D && t >= 0 && t < a.L;
+        p16_cp_async16(&sm.x[buf][r][8 * s], ok ? u + ((size_t)b * a.D + d) * a.L + t : u, ok);
+    }
+    for (int i = tid; i < kCh * kP16Segs; i += kP16Threads) {
+        const int r = i / kP16Segs, s = i - r * kP16Segs;
+        const int d = ch0 + r;
+        const int t = c0 + 8 * s;
+        const bool ok = d < a.D && t < a.L;
+        const size_t off = ((size_t)b * a.D + d) * a.L + t;
+        p16_cp_async16(&sm.dl[buf][r][kP16Halo + 8 * s], ok ? dl + off : dl, ok);
+        if (want_z) p16_cp_async16(&sm.zz[buf][r][kP16Halo + 8 * s], ok ? zz + off : zz, ok);
+    }
+    const uint16_t* Bm = static_cast<const uint16_t*>(a.Bm);
+    const uint16_t* Cm = static_cast<const uint16_t*>(a.Cm);
+    for (int i = tid; i < 2 * a.N * kP16Segs; i += kP16Threads) {
+        const int w = i / (a.N * kP16Segs);
+        const int rem = i - w * a.N * kP16Segs;
+        const int n = rem / kP16Segs, s = rem - n * kP16Segs;
+        const int t = c0 + 8 * s;
+        const bool ok = t < a.L;
+        const uint16_t* base = w ? Cm : Bm;
+        p16_cp_async16(&sm.bcr[buf][w][n][8 * s], ok ? base + ((size_t)b * a.N + n) * a.L + t : base, ok);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Per-lane constants: lane e of a channel holds states [e NSL, (e+1) NSL); pair p = states (2p, 2p+1)
+// of that range.
+template <int NSL>
+struct P16Consts {
+    f32x2 al2[NSL / 2];   // A log2(e)
+    f32x2 ninv[NSL / 2];  // -1/A (0 where A == 0 or padding; padding has B = C = 0)
+};
+
+// 8 steps starting at chunk column j0 (all inside [t_begin, t_end)).
+template <int NS, int LPC, Disc kDisc, bool kFinal, bool kConv>
+__device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem<NS, LPC>& sm, int buf, int j0,
+                                          const P16Consts<NS / LPC>& cc, const float (&w)[4], float cb, float dskip,
+                                          float bias, f32x2 (&hp)[NS / LPC / 2], float& dsum, bool has_z,
+                                          bool active, size_t yoff) {
+    constexpr int NSL = NS / LPC;   // states per lane
+    constexpr int SPL = 8 / LPC;    // steps whose scalars this lane owns
+    const int lane = threadIdx.x & 31;
+    const int e = lane & (LPC - 1);
+    const int r = threadIdx.x / LPC;          // channel within the block
+    const int src0 = lane & ~(LPC - 1);       // first lane of this channel
+    const int col = kP16Halo + j0 + e * SPL;  // first owned step's column
+    // --- scalars of the owned steps: SSM input v (conv front end), step dt, gate ---
+    float xs[SPL], v[SPL], dto[SPL], gate[SPL];
+    const uint16_t* xrow = &sm.x[buf][r][col];
+#pragma unroll
+    for (int k = 0; k < SPL; k += 2) {
+        const uint32_t xw = *reinterpret_cast<const uint32_t*>(xrow + k);
+        xs[k] = bf16_lo(xw);
+        xs[k + 1] = bf16_hi(xw);
+    }
+    if (kConv) {
+        // two 4-byte reads: the owned steps start at an even column, not always at a multiple of 4
+        const uint32_t hw0 = *reinterpret_cast<const uint32_t*>(xrow - 4);
+        const uint32_t hw1 = *reinterpret_cast<const uint32_t*>(xrow - 2);
+        const float h3 = bf16_hi(hw0), h2 = bf16_lo(hw1), h1 = bf16_hi(hw1);  // x_{t-3}, x_{t-2}, x_{t-1}
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) {
+            const float xm3 = k >= 3 ? xs[k - 3] : (k == 0 ? h3 : (k == 1 ? h2 : h1));
+            const float xm2 = k >= 2 ? xs[k - 2] : (k == 0 ? h2 : h1);
+            const float xm1 = k >= 1 ? xs[k - 1] : h1;
+            float c = fmaf(w[0], xm3, cb);
+            c = fmaf(w[1], xm2, c);
+            c = fmaf(w[2], xm1, c);
+            c = fmaf(w[3], xs[k], c);
+            v[k] = silu_fast(c);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) v[k] = xs[k];
+    }
+    {
+        const uint16_t* drow = &sm.dl[buf][r][col];
+#pragma unroll
+        for (int k = 0; k < SPL; k += 2) {
+            const uint32_t dw = *reinterpret_cast<const uint32_t*>(drow + k);
+            dto[k] = bf16_lo(dw) + bias;
+            dto[k + 1] = bf16_hi(dw) + bias;
+        }
+#pragma unroll
+        for (int k = 0; k < SPL; ++k)
+            if (a.softplus) dto[k] = softplus_fast(dto[k]);
+    }
+    if (kFinal) {
+        if (has_z) {
+            const uint16_t* zrow = &sm.zz[buf][r][col];
+#pragma unroll
+            for (int k = 0; k < SPL; k += 2) {
+                const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + k);
+                gate[k] = silu_fast(bf16_lo(zw));
+                gate[k + 1] = silu_fast(bf16_hi(zw));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) gate[k] = 1.0f;
+        }
+    }
+
+    // --- the recurrence and the readout, step by step ---
+    float out[SPL];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float dtj, vj;
+        if (LPC == 1) {
+            dtj = dto[j];
+            vj = v[j];
+        } else {  // step j's scalars live in lane src0 + j / SPL, register j % SPL
+            dtj = __shfl_sync(0xffffffffu, dto[j % SPL], src0 + j / SPL);
+            vj = __shfl_sync(0xffffffffu, v[j % SPL], src0 + j / SPL);
+        }
+        const f32x2 dt2 = pack2(dtj, dtj);
+        const f32x2 v2 = pack2(vj, vj);
+        const float* Bt = sm.bc[j0 + j][0] + e * NSL;
+        const float* Ct = sm.bc[j0 + j][1] + e * NSL;
+        f32x2 acc = pack2(0.0f, 0.0f);
+#pragma unroll
+        for (int p4 = 0; p4 < NSL / 2; p4 += 2) {
+            const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(Bt + 2 * p4);
+            const f32x2 Bp[2] = {bq.x, bq.y};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int p = p4 + q;
+                const f32x2 ab = ex2x2(mul2(dt2, cc.al2[p]));
+                if (kDisc == Disc::kSimple) {
+                    hp[p] = fma2(ab, hp[p], mul2(mul2(dt2, v2), Bp[q]));
+                } else if (kDisc == Disc::kZOH) {
+                    const f32x2 ng = mul2(mul2(v2, cc.ninv[p]), Bp[q]);
+                    hp[p] = fma2(ab, sub2(hp[p], ng), ng);
+                } else {  // Bbar = ([a == 0] dt - (Abar - 1) ninv) B
+                    float n0, n1;
+                    unpack2(cc.ninv[p], n0, n1);
+                    const f32x2 zdt = pack2(n0 == 0.0f ? dtj : 0.0f, n1 == 0.0f ? dtj : 0.0f);
+                    const f32x2 phi = sub2(zdt, mul2(sub2(ab, pack2(1.0f, 1.0f)), cc.ninv[p]));
+                    hp[p] = fma2(ab, hp[p], mul2(mul2(phi, Bp[q]), v2));
+                }
+            }
+            if (kFinal) {
+                const ulonglong2 cq = *reinterpret_cast<const ulonglong2*>(Ct + 2 * p4);
+                acc = fma2(cq.x, hp[p4], acc);
+                acc = fma2(cq.y, hp[p4 + 1], acc);
+            }
+        }
+        if (kFinal) {
+            float ya, yb;
+            unpack2(acc, ya, yb);
+            float y = ya + yb;
+#pragma unroll
+            for (int m = 1; m < LPC; m <<= 1) y += __shfl_xor_sync(0xffffffffu, y, m);
+            if (j / SPL == e) out[j % SPL] = y;
+        } else {
+            dsum += dtj;
+        }
+    }
+    if (kFinal && active) {
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) out[k] = fmaf(dskip, v[k], out[k]) * gate[k];
+        uint16_t* y = static_cast<uint16_t*>(a.y) + yoff + j0 + e * SPL;
+        if constexpr (SPL == 8) {
+            store8<BF16>(a.y, yoff + j0, out);
+        } else if constexpr (SPL == 4) {
+            *reinterpret_cast<uint2*>(y) = make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
+        } else {
+            *reinterpret_cast<uint32_t*>(y) = pack_bf16x2(out[0], out[1]);
+        }
+    }
+}
+
+// Resident blocks per SM the register budget aims at, by lanes per channel.
+__host__ __device__ constexpr int p16_min_blocks(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
+
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv>
+__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_kernel(const ScanKernelArgs a) {
+    constexpr int NSL = NS / LPC;
+    constexpr int kCh = P16Smem<NS, LPC>::kCh;
+    extern __shared__ __align__(16) unsigned char p16_smem_raw[];
+    P16Smem<NS, LPC>& sm = *reinterpret_cast<P16Smem<NS, LPC>*>(p16_smem_raw);
+    const int tid = threadIdx.x;
+    const int e = tid & (LPC - 1);
+    const int b = blockIdx.y, seg = blockIdx.z;
+    const int ch0 = blockIdx.x * kCh;
+    const int d = ch0 + tid / LPC;
+    const bool active = d < a.D;
+    const size_t rows = (size_t)a.Bsz * a.D;
+    const size_t row = (size_t)b * a.D + (active ? d : 0);
+    const int t_begin = seg * a.seg_len;
+    const int t_end = min(a.L, t_begin + a.seg_len);
+    const bool has_z = kFinal && a.z != nullptr;
+
+    // B/C rows past N stay zero (cp.async never writes them)
+    for (int i = tid; i < 2 * 2 * NS * kP16Row; i += kP16Threads) (&sm.bcr[0][0][0][0])[i] = 0;
+    __syncthreads();
+    p16_issue_chunk<NS, LPC>(a, sm, 0, b, ch0, t_begin, has_z);
+
+    P16Consts<NSL> cc;
+    bool has_zero = false;
+#pragma unroll
+    for (int p = 0; p < NSL / 2; ++p) {
+        float al[2], ni[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int n = e * NSL + 2 * p + q;
+            const bool real = active && n < a.N;
+            const float av = real ? __ldg(a.A + (size_t)d * a.N + n) : 0.0f;
+            al[q] = av * kLog2e;
+            ni[q] = av != 0.0f ? -1.0f / av : 0.0f;
+            has_zero |= real && av == 0.0f;
+        }
+        cc.al2[p] = pack2(al[0], al[1]);
+        cc.ninv[p] = pack2(ni[0], ni[1]);
+    }
+    float w[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float cb = 0.0f;
+    if (kConv && active) {
+        const int W = a.conv_width;
+        const float* cw = a.conv_w + (size_t)d * W;
+        // tap i of the 4-wide window is tap i - (4 - W) of the filter
+        w[0] = W >= 4 ? __ldg(cw + 0 - (4 - W)) : 0.0f;
+        w[1] = W >= 3 ? __ldg(cw + 1 - (4 - W)) : 0.0f;
+        w[2] = W >= 2 ? __ldg(cw + 2 - (4 - W)) : 0.0f;
+        w[3] = __ldg(cw + 3 - (4 - W));
+        if (a.conv_b != nullptr) cb = __ldg(a.conv_b + d);
+    }
+    const float dskip = (a.Dskip != nullptr && active) ? __ldg(a.Dskip + d) : 0.0f;
+    const float bias = (a.delta_bias != nullptr && active) ? __ldg(a.delta_bias + d) : 0.0f;
+
+    // this lane's states are n0 + i, i < NSL
+    const int n0 = e * NSL;
+    float h[NSL];
+#pragma unroll
+    for (int i = 0; i < NSL; ++i) h[i] = 0.0f;
+    float dsum = 0.0f;
+    if (kFinal) {
+        const float* h0 = (a.nseg > 1) ? a.ws_h0 : a.h0;
+        if (h0 != nullptr && active) {
+#pragma unroll
+            for (int i = 0; i < NSL; ++i)
+                if (n0 + i < a.N) h[i] = h0[row * a.N + n0 + i];
+        }
+        for (int s = 0; s < seg; ++s) {
+            const float S = active ? a.ws_dsum[(size_t)s * rows + row] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < NSL; ++i) {
+                float al0, al1;
+                unpack2(cc.al2[i / 2], al0, al1);
+                const float hs = (active && n0 + i < a.N) ? a.ws_h[((size_t)s * rows + row) * a.N + n0 + i] : 0.0f;
+                h[i] = fmaf(ex2((i & 1 ? al1 : al0) * S), h[i], hs);
+            }
+        }
+    } else if (seg == 0 && a.ws_h0 != nullptr && a.h0 != nullptr && active) {
+#pragma unroll
+        for (int i = 0; i < NSL; ++i)
+            if (n0 + i < a.N) a.ws_h0[row * a.N + n0 + i] = a.h0[row * a.N + n0 + i];
+    }
+    f32x2 hp[NSL / 2];
+#pragma unroll
+    for (int p = 0; p < NSL / 2; ++p) hp[p] = pack2(h[2 * p], h[2 * p + 1]);
+
+    const bool safe = kZOH && __syncthreads_or(has_zero);  // block-uniform choice of loop body
+    const size_t yoff = row * (size_t)a.L;
+
+    int buf = 0;
+    for (int c0 = t_begin; c0 < t_end; c0 += kP16Chunk, buf ^= 1) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();  // chunk c0 landed for every thread; everyone is done with the other buffers
+        if (c0 + kP16Chunk < t_end) p16_issue_chunk<NS, LPC>(a, sm, buf ^ 1, b, ch0, c0 + kP16Chunk, has_z);
+        // widen B / C of this chunk to fp32 (consecutive threads write consecutive floats)
+        for (int i = tid; i < 2 * NS * kP16Chunk; i += kP16Threads) {
+            const int t = i / (2 * NS);
+            const int rem = i - t * 2 * NS;
+            const int wv = rem / NS, n = rem - wv * NS;
+            sm.bc[t][wv][n] = bf16_to_f32(sm.bcr[buf][wv][n][t]);
+        }
+        __syncthreads();
+        const int clen = min(kP16Chunk, t_end - c0);
+        // every lane of a warp takes part (the shuffles need them); inactive channels write nothing
+        for (int j0 = 0; j0 < clen; j0 += 8) {
+            if (safe)
+                p16_group<NS, LPC, Disc::kZOHSafe, kFinal, kConv>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum, has_z,
+                                                                   active, yoff + c0);
+            else
+                p16_group<NS, LPC, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv>(a, sm, buf, j0, cc, w, cb, dskip,
+                                                                                   bias, hp, dsum, has_z, active,
+                                                                                   yoff + c0);
+        }
+    }
+
+    if (!active) return;
+#pragma unroll
+    for (int p = 0; p < NSL / 2; ++p) unpack2(hp[p], h[2 * p], h[2 * p + 1]);
+    if (kFinal) {
+        if (seg == a.nseg - 1 && a.h_out != nullptr) {
+#pragma unroll
+            for (int i = 0; i < NSL; ++i)
+                if (n0 + i < a.N) a.h_out[row * a.N + n0 + i] = h[i];
+        }
+    } else {
+        if (e == 0) a.ws_dsum[(size_t)seg * rows + row] = dsum;
+#pragma unroll
+        for (int i = 0; i < NSL; ++i)
+            if (n0 + i < a.N) a.ws_h[((size_t)seg * rows + row) * a.N + n0 + i] = h[i];
+    }
+}
+
+template <int NS, int LPC, bool kZOH, bool kConv>
+cudaError_t launch_p16_ns(const ScanKernelArgs& a, cudaStream_t stream) {
+    const size_t smem = sizeof(P16Smem<NS, LPC>);
+    constexpr int kCh = P16Smem<NS, LPC>::kCh;
+    dim3 block(kP16Threads);
+    const unsigned gx = (unsigned)((a.D + kCh - 1) / kCh);
+    cudaError_t e;
+    if (a.nseg > 1) {
+        auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv>;
+        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    auto kfn = scan_p16_kernel<NS, LPC, kZOH, true, kConv>;
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int NS, int LPC>
+cudaError_t launch_p16(const ScanKernelArgs& a, int zoh, cudaStream_t s) {
+    const bool conv = a.conv_w != nullptr;
+    if (zoh) return conv ? launch_p16_ns<NS, LPC, true, true>(a, s) : launch_p16_ns<NS, LPC, true, false>(a, s);
+    return conv ? launch_p16_ns<NS, LPC, false, true>(a, s) : launch_p16_ns<NS, LPC, false, false>(a, s);
+}
+
+}  // namespace ssm

@@ -10,6 +10,10 @@ namespace ssm {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Discretisation of the input term: zero-order hold, zero-order hold with A == 0 entries present in
+// the warp (uses the dt * B limit there), or the simplified dt * B.
+enum class Disc { kZOH, kZOHSafe, kSimple };
+
 // 2^x on the MUFU unit (ex2.approx.ftz: about 2 ulp, 32 results per clock per SM on B300).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -50,6 +54,70 @@ __device__ __forceinline__ float softplus(float s) {
 // the reciprocal gives 0, the correctly rounded limit.
 __device__ __forceinline__ float silu(float v) {
     return v * rcp(1.0f + ex2(-v * kLog2e));
+}
+
+// Variants for bf16 outputs (whose rounding is 2^-9): they move work from the FMA pipe to the
+// MUFU, which the scan kernels have to spare.
+// tanh on the MUFU (tanh.approx: relative error about 1e-5, 16 results per clock per SM on B300).
+__device__ __forceinline__ float tanh_mufu(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// log2 on the MUFU (lg2.approx: absolute error about 2e-7 near 1).
+__device__ __forceinline__ float lg2_mufu(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// SiLU(v) = v sigmoid(v) = h + h tanh(h) with h = v / 2.
+__device__ __forceinline__ float silu_fast(float v) {
+    const float hv = 0.5f * v;
+    return fmaf(hv, tanh_mufu(hv), hv);
+}
+// softplus(s) = max(s, 0) + ln2 * log2(1 + 2^(-|s| log2 e)); absolute error about 2e-7.
+__device__ __forceinline__ float softplus_fast(float s) {
+    const float e = ex2(-fabsf(s) * kLog2e);
+    return fmaf(lg2_mufu(1.0f + e), kLn2, fmaxf(s, 0.0f));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Packed pairs of fp32 (sm_100+ f32x2 instructions): one issue slot for two lanes of FMA-pipe work.
+// ---------------------------------------------------------------------------------------------
+using f32x2 = unsigned long long;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f32x2 ex2x2(f32x2 x) {
+    float a, b;
+    unpack2(x, a, b);
+    return pack2(ex2(a), ex2(b));
 }
 
 // ---------------------------------------------------------------------------------------------

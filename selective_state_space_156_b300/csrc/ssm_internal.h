@@ -34,7 +34,13 @@ struct ScanKernelArgs {
     float* ws_h;     // (nseg - 1, B*D, N) end state of each segment but the last, from a zero start
     float* ws_dsum;  // (nseg - 1, B*D) sum of dt over each segment but the last
     float* ws_h0;    // (B*D, N) copy of h0 taken before any block may write h_out (h0 may alias h_out)
+    int kind;        // kScanSeq, kScanP16 or kScanG4
+    int lpc;         // kScanP16: lanes per channel (1, 2 or 4)
 };
+
+constexpr int kScanSeq = 0;  // one (b, d) row per thread, all states in registers (any dtype, any alignment)
+constexpr int kScanP16 = 2;  // one row per thread, cp.async staging, packed fp32 pairs (bf16, aligned, N <= 16)
+constexpr int kScanG4 = 1;   // four lanes per channel, tensor-core readout (bf16, aligned, 16 < N <= 64)
 
 constexpr int kScanThreads = 128;  // channels per block in the scan kernels
 constexpr int kScanChunk = 64;     // timesteps of B/C staged in shared memory at a time
@@ -48,6 +54,11 @@ cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, 
 cudaError_t launch_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
                                 const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
                                 int Bsz, int D, int N, int softplus, int zoh, int dtype, cudaStream_t stream);
+
+// Launch geometry of each kernel kind, used by the host to plan the L split.
+constexpr int kSeqChanPerBlock = 128, kSeqBlocksPerSM = 3, kSeqChunk = 64;
+constexpr int kG4ChanPerBlock = 32, kG4BlocksPerSM = 7, kG4ChunkSteps = 32;
+constexpr int kP16Threads_ = 128, kP16ChunkSteps = 32;  // kScanP16: channels per block = 128 / lpc
 
 // Per-dtype-combination entry points defined in scan_<in>_<out>.cu.
 cudaError_t launch_scan_f32_f32(const ScanKernelArgs& a, int zoh, cudaStream_t s);

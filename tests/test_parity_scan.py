@@ -233,3 +233,60 @@ def test_full_long_context_sampled_and_chunk_split():
     y_chain = torch.cat(ys, dim=-1)
     assert_close(y_chain, y_ref, y_tolerance(y_ref, torch.bfloat16), "y (32 chained calls)")
     assert_close(h[0, di], h_ref, h_tolerance(h_ref, torch.bfloat16), "h (32 chained calls)")
+
+
+# ------------------------------------------------------------------------------------------------
+# The four-lanes-per-channel kernel (bf16 in and out, rows 16-byte aligned, L % 8 == 0)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("N", [1, 4, 7, 16, 32, 64])
+@pytest.mark.parametrize("L", [8, 40, 96])
+def test_g4_dstate_and_lengths(N, L):
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba130m"], batch=2, dim=70, seqlen=L, dstate=N,
+                                   with_h0=True)
+    check_full(d)
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 4])
+@pytest.mark.parametrize("zoh", [True, False])
+def test_g4_fused_conv(width, zoh):
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba1.4b_conv"], batch=2, dim=96, seqlen=200)
+    g = torch.Generator().manual_seed(17 + width)
+    d["conv_w"] = (torch.randn((96, width), generator=g) * 0.5).contiguous()
+    d["conv_b"] = torch.randn(96, generator=g) * 0.1
+    d["zoh"] = zoh
+    check_full(d)
+
+
+@pytest.mark.parametrize("has_z,has_D,softplus", [(False, True, True), (True, False, True), (True, True, False)])
+def test_g4_flags(has_z, has_D, softplus):
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba130m"], batch=3, dim=40, seqlen=128, with_h0=True)
+    if not has_z:
+        d["z"] = None
+    if not has_D:
+        d["Dskip"] = None
+    if not softplus:
+        d["delta_softplus"] = False
+        d["delta"] = (d["delta"].float().abs() * 0.05 + 1e-3).to(torch.bfloat16)
+        d["delta_bias"] = None
+    check_full(d)
+
+
+def test_g4_zero_A():
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba130m"], batch=2, dim=64, seqlen=64, with_h0=True)
+    A = d["A"].clone()
+    A[5, :] = 0.0
+    A[33, 7] = 0.0
+    d["A"] = A
+    check_full(d)
+
+
+@pytest.mark.parametrize("N", [16, 64])
+def test_g4_split_with_aliased_state(N):
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["long2.8b"], batch=1, dim=64, seqlen=6144, dstate=N,
+                                   with_h0=True)
+    g = to_dev(d)
+    assert ssm.ssm_scan_workspace_size(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g["h0"], z=g["z"]) > 0
+    y_ref, h_ref, _ = oracle.scan(d)
+    y, h = run_gpu(d, workspace="auto", alias_state=True)
+    assert_close(y, y_ref.reshape(y.shape), y_tolerance(y_ref.reshape(y.shape), torch.bfloat16), "y")
+    assert_close(h, h_ref.reshape(h.shape), h_tolerance(h_ref.reshape(h.shape), torch.bfloat16), "h_out")
