@@ -21,7 +21,11 @@ template <int OP>
 __device__ __forceinline__ float op(float x) {
     float y;
     if (OP == 0) asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    if (OP == 1) asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    if (OP == 1) {  // x -> 1 / (x + 1): the add keeps the chain from folding to the identity
+        float t;
+        asm volatile("add.f32 %0, %1, 0f3F800000;" : "=f"(t) : "f"(x));
+        asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+    }
     if (OP == 2) asm volatile("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     if (OP == 3) asm volatile("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     if (OP == 4) asm volatile("fma.rn.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(x), "f"(0.99991f), "f"(1e-4f));
