@@ -121,6 +121,27 @@ typedef struct ssm_scan_params {
    conv_width outside 1..4), SSM_ERR_UNSUPPORTED (dstate not supported), SSM_ERR_CUDA. */
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream);
 
+/*
+ * ssm_scan_fwd without any allocation.  (No counterpart on the pages: this is an interface for
+ * callers of this library.)  Some callers cannot call cudaMalloc: a serving runtime that plans all
+ * device memory at start-up and forbids allocation afterwards, code running in a stream callback or
+ * host function (where CUDA calls are not allowed), or latency-critical paths where an allocation
+ * may synchronise the device and stall other streams.  This entry point computes exactly what
+ * ssm_scan_fwd computes with a large enough workspace, but takes the scratch for the L split from a
+ * fixed 4 MiB buffer inside the library (p->workspace and p->workspace_bytes are ignored).  The
+ * caller still provides every input and output.
+ *   - The buffer lives in each device's memory from the first use until the process exits.
+ *   - The first call on a device looks up the buffer's device address (once per device, with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call shares the one buffer per device: calls whose kernels may overlap on the GPU
+ *     (different streams, or several host threads) race on it and must be serialised by the caller.
+ *   - A problem whose split needs more than 4 MiB of scratch is rejected with SSM_ERR_UNSUPPORTED
+ *     and a message; nothing is launched.  Problems that need no split use no scratch at all.
+ * Errors: as ssm_scan_fwd, plus SSM_ERR_UNSUPPORTED for a problem beyond the buffer and SSM_ERR_CUDA
+ * if the device address cannot be obtained.
+ */
+SSM_API ssm_status ssm_scan_fwd_static(const ssm_scan_params *p, ssm_stream_t stream);
+
 /* Bytes of workspace that let ssm_scan_fwd split L for this problem on the current device
    (0 when no split would be used).  Returns 0 for an invalid p. */
 SSM_API size_t ssm_scan_workspace_size(const ssm_scan_params *p);

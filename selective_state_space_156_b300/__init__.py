@@ -19,7 +19,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssm_scan_fwd", "causal_conv1d_fwd", "ssm_state_update", "ssm_scan_workspace_size", "lib",
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_static", "causal_conv1d_fwd", "ssm_state_update", "ssm_scan_workspace_size", "lib",
            "SsmError", "ScanParams", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssm_b300.so")
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
         L.ssm_scan_fwd.restype = st
         L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), vp]
+        L.ssm_scan_fwd_static.restype = st
+        L.ssm_scan_fwd_static.argtypes = [ctypes.POINTER(ScanParams), vp]
         L.ssm_scan_workspace_size.restype = ctypes.c_size_t
         L.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
         L.causal_conv1d_fwd.restype = st
@@ -177,6 +179,27 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
     p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
                      workspace)
     _check(lib().ssm_scan_fwd(ctypes.byref(p), _stream(stream)))
+    return (y, h_out) if return_state else y
+
+
+def ssm_scan_fwd_static(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
+                        Dskip: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                        z: Optional[torch.Tensor] = None, conv_w: Optional[torch.Tensor] = None,
+                        conv_b: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
+                        h_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                        delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
+                        return_state: bool = False, stream=None):
+    """ssm_scan_fwd for callers that cannot allocate scratch: the L split uses the library's fixed
+    4 MiB device buffer instead of a workspace.  Calls that may overlap on the GPU share that buffer and
+    must be serialised.  Output tensors are allocated here only when not given (pass y / h_out to keep
+    the call allocation-free)."""
+    if y is None:
+        y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
+    if return_state and h_out is None:
+        h_out = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+    p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
+                     None)
+    _check(lib().ssm_scan_fwd_static(ctypes.byref(p), _stream(stream)))
     return (y, h_out) if return_state else y
 
 

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <mutex>
 #include <string>
 
 #include "ssm_internal.h"
@@ -159,6 +160,44 @@ ssm_status validate_scan(const ssm_scan_params* p) {
     return SSM_OK;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Scratch for ssm_scan_fwd_static: a fixed buffer in the library's own device memory, for callers
+// that cannot allocate.  Every GPU that loads the library holds these bytes until the process exits.
+// ---------------------------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = (size_t)4 << 20;  // 4 MiB
+constexpr int kStaticScratchMaxDevices = 64;
+
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kStaticScratchMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char ssm_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+// Device address of ssm_static_scratch on the current device.  The host-side name of the array is
+// only a stand-in, so the address is asked of the runtime once per device, with that device current,
+// and cached.
+ssm_status static_scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "ssm_scan_fwd_static: cudaGetDevice");
+    if (dev < 0 || dev >= kStaticScratchMaxDevices)
+        return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd_static: device %d is beyond the %d devices it tracks", dev,
+                    kStaticScratchMaxDevices);
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_addr[dev] == nullptr) {
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, ssm_static_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "ssm_scan_fwd_static: cudaGetSymbolAddress");
+        if (addr == nullptr) return fail(SSM_ERR_CUDA, "ssm_scan_fwd_static: no device address for the scratch buffer");
+        g_static_scratch_addr[dev] = addr;
+    }
+    *out = g_static_scratch_addr[dev];
+    return SSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -245,6 +284,47 @@ ssm_status ssm_state_update(float* state, const void* u, const void* delta, cons
     return cuda_status(ssm::launch_state_update(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, batch, dim, dstate,
                                                 delta_softplus, zoh, (int)dtype, (cudaStream_t)stream),
                        "ssm_state_update launch");
+}
+
+ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
+    ssm_status st = validate_scan(p);
+    if (st != SSM_OK) return st;
+
+    ssm::ScanKernelArgs a{};
+    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
+    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm;
+    a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
+    a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
+    a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
+    a.softplus = p->delta_softplus;
+    a.vec = aligned_rows(p);
+    a.kind = scan_kind(p);
+    a.lpc = choose_lpc(p);
+
+    // the same launch plan as ssm_scan_fwd with a large enough workspace; p->workspace is ignored
+    const SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
+    const size_t need = workspace_bytes_for(p, sp);
+    if (need > kStaticScratchBytes)
+        return fail(SSM_ERR_UNSUPPORTED,
+                    "ssm_scan_fwd_static: this problem needs %zu bytes of scratch, more than the %zu-byte static "
+                    "buffer; call ssm_scan_fwd with a caller workspace instead",
+                    need, kStaticScratchBytes);
+    a.nseg = sp.nseg;
+    a.seg_len = sp.seg_len;
+    if (sp.nseg > 1) {
+        // Nothing here has to start at zero: the summary pass of this call writes every word of the
+        // scratch that its final pass reads (segment sums, segment end states, the copy of h0).
+        void* base = nullptr;
+        st = static_scratch_address(&base);
+        if (st != SSM_OK) return st;
+        const size_t rows = (size_t)p->batch * p->dim;
+        float* w = reinterpret_cast<float*>(base);
+        a.ws_dsum = w;
+        a.ws_h = w + (size_t)(sp.nseg - 1) * rows;
+        a.ws_h0 = p->h0 != nullptr ? a.ws_h + (size_t)(sp.nseg - 1) * rows * p->dstate : nullptr;
+    }
+    return cuda_status(ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream),
+                       "ssm_scan_fwd_static launch");
 }
 
 }  // extern "C"
