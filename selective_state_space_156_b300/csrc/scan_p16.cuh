@@ -144,29 +144,28 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
         for (int k = 0; k < SPL; ++k) v[k] = xs[k];
     }
     {
+        // branch-free (compute, then select): the group stays one basic block, so the scheduler can
+        // overlap these MUFU-heavy scalars with the FMA-heavy steps below
         const uint16_t* drow = &sm.dl[buf][r][col];
+        const bool sp_on = a.softplus != 0;
 #pragma unroll
         for (int k = 0; k < SPL; k += 2) {
             const uint32_t dw = *reinterpret_cast<const uint32_t*>(drow + k);
-            dto[k] = bf16_lo(dw) + bias;
-            dto[k + 1] = bf16_hi(dw) + bias;
+            const float s0 = bf16_lo(dw) + bias, s1 = bf16_hi(dw) + bias;
+            const float p0 = softplus_fast(s0), p1 = softplus_fast(s1);
+            dto[k] = sp_on ? p0 : s0;
+            dto[k + 1] = sp_on ? p1 : s1;
         }
-#pragma unroll
-        for (int k = 0; k < SPL; ++k)
-            if (a.softplus) dto[k] = softplus_fast(dto[k]);
     }
     if (kFinal) {
-        if (has_z) {
-            const uint16_t* zrow = &sm.zz[buf][r][col];
+        // without z the staged z rows hold stale values; the select (not a product) keeps them out
+        const uint16_t* zrow = &sm.zz[buf][r][col];
 #pragma unroll
-            for (int k = 0; k < SPL; k += 2) {
-                const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + k);
-                gate[k] = silu_fast(bf16_lo(zw));
-                gate[k + 1] = silu_fast(bf16_hi(zw));
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < SPL; ++k) gate[k] = 1.0f;
+        for (int k = 0; k < SPL; k += 2) {
+            const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + k);
+            const float g0 = silu_fast(bf16_lo(zw)), g1 = silu_fast(bf16_hi(zw));
+            gate[k] = has_z ? g0 : 1.0f;
+            gate[k + 1] = has_z ? g1 : 1.0f;
         }
     }
 
