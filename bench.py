@@ -7,8 +7,10 @@ softplus step, zero-order-hold discretisation, scan, C readout, D skip and SiLU 
 kernel launch.  Inputs are seeded synthetic tensors resident in HBM before the timed region.
 
 Prints ONE JSON line (rank 0).  Keys beyond the base contract:
-  roofline      dominant kernel vs its ALU (MUFU) roof: algorithmic transcendental ops per launch
-                / CUDA-event launch time, against 148 SMs x measured ex2 rate/clk x max SM clock
+  roofline      dominant kernel vs the binding one of three roofs, each algorithmic work per launch /
+                CUDA-event launch time: FP32 lane ops (148 SMs x 128 lanes x max SM clock), MUFU
+                transcendentals (148 SMs x measured ex2 rate/clk x max SM clock), HBM bytes (measured
+                copy bandwidth); all three are listed under "terms"
   hbm           the same launch against the measured HBM copy bandwidth
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload, host cores
   e2e           the same metric through the public API with pinned host buffers, copies included
@@ -42,6 +44,7 @@ METRIC = "scan elems/s (B*D*L*N)"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
 MAX_SM_MHZ = 2032.0
+FP32_LANES_PER_SM = 128   # FP32 FMA lanes per SM (4 sub-partitions x 32)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -65,6 +68,15 @@ def scan_mufu_ops(cfg) -> int:
     (exp + reciprocal)."""
     per = cfg.dstate + 2 + (2 if cfg.has_z else 0) + (2 if cfg.conv else 0)
     return per * cfg.batch * cfg.dim * cfg.seqlen
+
+
+def scan_fp32_ops(cfg) -> int:
+    """FP32-pipe lane operations the recurrence needs per element (b, d, t, n), counting a fused
+    multiply-add as one: the exponent argument dt*A; with zero-order hold the input term v*(-1/A)*B (two
+    products), the update Abar*(h - g) + g (a difference and an FMA) and the readout FMA, 6 in all; with
+    the simplified B*dt*v (dt*v shared by the N states), one product, one FMA and the readout FMA, 4.
+    The per-(b, d, t) work (softplus, conv, gate) is not counted."""
+    return (6 if cfg.zoh else 4) * cfg.elements
 
 
 def measured_peaks() -> dict:
@@ -174,7 +186,16 @@ def dist_env():
 
 def shard_batches(total_ranks: int, rank: int, per_rank_batch: int):
     """Weak scaling: rank r owns global batch rows [r * per_rank_batch, (r + 1) * per_rank_batch)."""
+    if not 0 <= rank < total_ranks:
+        raise ValueError(f"rank {rank} outside [0, {total_ranks})")
     return range(rank * per_rank_batch, (rank + 1) * per_rank_batch)
+
+
+def rank_inputs(cfg, rank: int) -> dict:
+    """Rank r's shard of the global batch: its own batch rows (u/x, delta, z, B, C drawn from a seed of
+    its own) and the one layer's parameters every rank shares (A, D skip, dt bias, conv filter).  Rows
+    are independent recurrences, so the shards need no exchange."""
+    return workloads.make_scan_inputs(cfg, seed=cfg.seed + 7919 * rank, params_seed=cfg.seed)
 
 
 def barrier(world):
@@ -183,11 +204,30 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time, on every rank (a collective on the timing only, never on data)."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (ms_slowest * 1e-3)
+
+
+def config_dict(cfg, world: int) -> dict:
+    return {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} "
+                        f"L={cfg.seqlen} {cfg.dtype} I/O, fp32 state"
+                        + (", fused conv1d(k=4)+SiLU" if cfg.conv else "")
+                        + (", ZOH" if cfg.zoh else ", B*dt") + (", D skip" if cfg.has_D else "")
+                        + (", SiLU(z) gate" if cfg.has_z else ""),
+            "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
+            "parallelism": f"replicas x{world} (batch shards, no collective)",
+            "l2": f"256 MB buffer written between timed steps, outside the events; inputs "
+                  f"{scan_bytes(cfg) / 1e6:.0f} MB"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -225,7 +265,7 @@ def run_b300(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = workloads.SCAN_CONFIGS[args.workload]
-    cpu_inputs = workloads.make_scan_inputs(cfg, seed=cfg.seed + 7919 * rank)
+    cpu_inputs = rank_inputs(cfg, rank)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu_inputs.items()}
     y = torch.empty_like(g["u"])
     h_out = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
@@ -266,7 +306,7 @@ def run_b300(args, rank, world, local):
     ms_local = statistics.fmean(times)
     ms = max_over_ranks(ms_local, world)
     elements = cfg.elements
-    value = world * elements / (ms * 1e-3)
+    value = aggregate_rate(elements, world, ms)
 
     # --- end to end through the public API with pinned host buffers ---
     e2e = None
@@ -299,7 +339,7 @@ def run_b300(args, rank, world, local):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b) / E, world)
-        e2e = {"value": world * elements / (e2e_ms * 1e-3), "unit": "elem/s", "ms_per_step": e2e_ms,
+        e2e = {"value": aggregate_rate(elements, world, e2e_ms), "unit": "elem/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E}
 
     # --- roofline of the dominant (only) kernel ---
@@ -310,13 +350,29 @@ def run_b300(args, rank, world, local):
     rate_clk, probe = mufu_rate_per_clk(not args.no_peaks) if rank == 0 else (32.0, {})
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mufu_peak = sms * rate_clk * MAX_SM_MHZ * 1e6           # ex2-class ops / s
+    fp32_peak = sms * FP32_LANES_PER_SM * MAX_SM_MHZ * 1e6  # FP32 lane operations / s
     mufu_ops = scan_mufu_ops(cfg)
+    fp32_ops = scan_fp32_ops(cfg)
     nbytes = scan_bytes(cfg)
     t_s = ms * 1e-3
-    roof = {"bound": "alu", "achieved": mufu_ops / t_s / 1e12, "peak": mufu_peak / 1e12, "unit": "Tmufu/s",
-            "frac": (mufu_ops / t_s) / mufu_peak, "traffic": args.traffic,
-            "peak_source": f"derived: {sms} SMs x {rate_clk:.1f} ex2/clk/SM (bench_peaks.cu) x {MAX_SM_MHZ:.0f} MHz",
-            "ops_per_launch": mufu_ops, "kernel": "scan_seq_kernel (final pass)"}
+    # the three roofs of the launch; the one with the longest ideal time binds
+    terms = {
+        "fp32": {"ideal_us": fp32_ops / fp32_peak * 1e6, "ops_per_launch": fp32_ops, "achieved": fp32_ops / t_s / 1e12,
+                 "peak": fp32_peak / 1e12, "unit": "TFLOP/s (FP32 lane ops)",
+                 "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {MAX_SM_MHZ:.0f} MHz"},
+        "mufu": {"ideal_us": mufu_ops / mufu_peak * 1e6, "ops_per_launch": mufu_ops, "achieved": mufu_ops / t_s / 1e12,
+                 "peak": mufu_peak / 1e12, "unit": "Tmufu/s",
+                 "peak_source": f"derived: {sms} SMs x {rate_clk:.1f} ex2/clk/SM (bench_peaks.cu) x {MAX_SM_MHZ:.0f} MHz"},
+        "hbm": {"ideal_us": nbytes / (hbm_peak * 1e9) * 1e6, "bytes_per_launch": nbytes, "achieved": nbytes / t_s / 1e9,
+                "peak": hbm_peak, "unit": "GB/s", "peak_source": f"{hbm_src} (MEASURED_PEAKS.json hbm_gbs)"},
+    }
+    bind = max(terms, key=lambda k: terms[k]["ideal_us"])
+    tb = terms[bind]
+    roof = {"bound": "hbm" if bind == "hbm" else "alu", "pipe": bind, "achieved": tb["achieved"], "peak": tb["peak"],
+            "unit": tb["unit"], "frac": tb["achieved"] / tb["peak"], "traffic": args.traffic,
+            "peak_source": tb["peak_source"], "kernel": "scan_p16_kernel (final pass)",
+            "terms": {k: {kk: vv for kk, vv in v.items() if kk != "peak_source"} | {"frac": v["achieved"] / v["peak"]}
+                      for k, v in terms.items()}}
     hbm = {"achieved_gbs": nbytes / t_s / 1e9, "peak_gbs": hbm_peak, "frac": nbytes / t_s / 1e9 / hbm_peak,
            "bytes_per_launch": nbytes, "peak_source": hbm_src}
 
@@ -337,12 +393,8 @@ def run_b300(args, rank, world, local):
         line = {
             "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} "
-                                   f"L={cfg.seqlen} bf16 I/O, fp32 state, fused conv1d(k=4)+SiLU, ZOH, D skip, "
-                                   "SiLU(z) gate", "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
-                       "parallelism": f"replicas x{world} (batch shards, no collective)",
-                       "l2": "256 MB buffer written between timed steps, outside the events; inputs 538 MB"},
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(cfg, world),
             "gpu_launches": K * launches_per_step,
             "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
             "clocks": clk.summary(), "wall_s_timed_region": wall, "mufu_probe": probe,
@@ -407,7 +459,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     cfg = workloads.SCAN_CONFIGS[args.workload]
-    d = workloads.make_scan_inputs(cfg)
+    d = rank_inputs(cfg, 0)
     budget = 150.0  # seconds for the whole --steps K --warmup W run
     rate0, nt, R0, secs0 = oracle_rate(d, 2.0)
     per_step_s = min(5.0, budget / max(1, args.steps + args.warmup))
@@ -428,9 +480,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} "
-                                   f"L={cfg.seqlen}", "global_batch": cfg.batch, "seq_len": cfg.seqlen,
-                       "parallelism": "host threads over (b, d) rows"},
+            "config": config_dict(cfg, 1),
             "cpu_baseline": {"value": value, "unit": "elem/s", "cores": nt, "kind": "oracle",
                              "sample": f"{len(sample)} random (b, d) rows per step of {R}, full L={cfg.seqlen}"},
             "e2e": {"value": value, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

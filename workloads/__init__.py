@@ -107,18 +107,22 @@ def _dt_bias(dim: int, kind: str, g: torch.Generator) -> torch.Tensor:
 
 def make_scan_inputs(cfg: ScanConfig, *, batch: Optional[int] = None, dim: Optional[int] = None,
                      seqlen: Optional[int] = None, dstate: Optional[int] = None, dtype: Optional[str] = None,
-                     with_h0: bool = False, seed: Optional[int] = None) -> dict:
+                     with_h0: bool = False, seed: Optional[int] = None,
+                     params_seed: Optional[int] = None) -> dict:
     """CPU tensors for one scan workload.  Overrides shrink or reshape the workload (parity edge cases)
-    while keeping the config's distributions."""
+    while keeping the config's distributions.  ``params_seed`` (default: the data seed) draws the
+    per-channel parameters (D skip, dt bias, conv filter) apart from the per-row tensors, so several
+    shards of one global batch can share one layer's parameters."""
     Bsz = cfg.batch if batch is None else batch
     D = cfg.dim if dim is None else dim
     L = cfg.seqlen if seqlen is None else seqlen
     N = cfg.dstate if dstate is None else dstate
     dt = _io_dtype(cfg.dtype if dtype is None else dtype)
     base = cfg.seed if seed is None else seed
+    pbase = base if params_seed is None else params_seed
 
-    def normal(tag, shape, std=1.0):
-        t = torch.randn(shape, generator=_gen(base, tag), dtype=torch.float32)
+    def normal(tag, shape, std=1.0, src=None):
+        t = torch.randn(shape, generator=_gen(base if src is None else src, tag), dtype=torch.float32)
         if std != 1.0:
             t.mul_(std)
         return t
@@ -130,10 +134,10 @@ def make_scan_inputs(cfg: ScanConfig, *, batch: Optional[int] = None, dim: Optio
     out["Bm"] = normal("B", (Bsz, N, L)).to(dt)
     out["Cm"] = normal("C", (Bsz, N, L)).to(dt)
     out["A"] = (-torch.arange(1, N + 1, dtype=torch.float32)).repeat(D, 1).contiguous()
-    out["Dskip"] = normal("D", (D,)) if cfg.has_D else None
-    out["delta_bias"] = _dt_bias(D, cfg.bias_kind, _gen(base, "bias"))
+    out["Dskip"] = normal("D", (D,), src=pbase) if cfg.has_D else None
+    out["delta_bias"] = _dt_bias(D, cfg.bias_kind, _gen(pbase, "bias"))
     if cfg.conv:
-        out["conv_w"] = normal("conv_w", (D, 4), 0.5)               # variance 1/4
+        out["conv_w"] = normal("conv_w", (D, 4), 0.5, src=pbase)    # variance 1/4
         out["conv_b"] = torch.zeros(D, dtype=torch.float32)
     else:
         out["conv_w"] = None
