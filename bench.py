@@ -79,6 +79,29 @@ def scan_fp32_ops(cfg) -> int:
     return (6 if cfg.zoh else 4) * cfg.elements
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one final-pass launch of the scan kernel on each
+# workload, from the ncu capture summarised under profiles/, keyed by the hash of the kernel sources it
+# was taken on: after any change to those sources the figure no longer applies and is reported as null.
+KERNEL_SOURCES = ("scan_p16.cuh", "ssm_device.cuh", "ssm_internal.h", "abi.cu")
+TRAFFIC = {"mamba1.4b_conv": (405092352 + 113960704, "ac28544e14a0b147")}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "selective_state_space_156_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str, override):
+    if override is not None:
+        return override
+    got = TRAFFIC.get(workload)
+    return got[0] if got and got[1] == kernel_source_hash() else None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -264,6 +287,12 @@ def run_b300(args, rank, world, local):
     import selective_state_space_156_b300 as ssm
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.decode_only:  # the decode workload alone (profiling runs; smaller with --decode-layers/steps)
+        hbm_peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+        decode = run_decode(ssm, dev, hbm_peak, world, steps=args.decode_steps, nlayers=args.decode_layers)
+        if rank == 0:
+            print(json.dumps({"decode": decode}), flush=True)
+        return
     cfg = workloads.SCAN_CONFIGS[args.workload]
     cpu_inputs = rank_inputs(cfg, rank)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu_inputs.items()}
@@ -369,7 +398,8 @@ def run_b300(args, rank, world, local):
     bind = max(terms, key=lambda k: terms[k]["ideal_us"])
     tb = terms[bind]
     roof = {"bound": "hbm" if bind == "hbm" else "alu", "pipe": bind, "achieved": tb["achieved"], "peak": tb["peak"],
-            "unit": tb["unit"], "frac": tb["achieved"] / tb["peak"], "traffic": args.traffic,
+            "unit": tb["unit"], "frac": tb["achieved"] / tb["peak"], "traffic": traffic_for(args.workload, args.traffic),
+            "kernel_source_hash": kernel_source_hash(),
             "peak_source": tb["peak_source"], "kernel": "scan_p16_kernel (final pass)",
             "terms": {k: {kk: vv for kk, vv in v.items() if kk != "peak_source"} | {"frac": v["achieved"] / v["peak"]}
                       for k, v in terms.items()}}
@@ -379,7 +409,7 @@ def run_b300(args, rank, world, local):
     # --- decode workload (ssm_state_update) ---
     decode = None
     if not args.no_decode:
-        decode = run_decode(ssm, dev, hbm_peak, world)
+        decode = run_decode(ssm, dev, hbm_peak, world, steps=args.decode_steps, nlayers=args.decode_layers)
 
     # --- CPU baseline: oracle on host cores, rank 0 at N = 1 only ---
     cpu = None
@@ -403,19 +433,20 @@ def run_b300(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_decode(ssm, dev, hbm_peak, world, steps=None):
+def run_decode(ssm, dev, hbm_peak, world, steps=None, nlayers=None):
     """64 layers x 128 tokens of ssm_state_update, layer-major per token, replayed as one CUDA graph per
     token.  Every layer keeps its own fp32 state cache (5.4 GB in total); per-token inputs come from a
     pool of 64 sets (512 MB), so neither states nor inputs can stay in L2 between uses."""
     cfg = workloads.DECODE_CONFIG
     P = 64
     steps = steps or cfg.steps
+    nl = nlayers or cfg.layers
     pool = workloads.make_decode_pool(cfg, P, device=dev)
-    layers = [workloads.make_decode_layer(cfg, l, device=dev) for l in range(cfg.layers)]
+    layers = [workloads.make_decode_layer(cfg, l, device=dev) for l in range(nl)]
     y = torch.empty((cfg.batch, cfg.dim), dtype=torch.bfloat16, device=dev)
 
     def token(step):
-        for l in range(cfg.layers):
+        for l in range(nl):
             k = workloads.decode_pool_index(l, step, P)
             L_ = layers[l]
             ssm.ssm_state_update(L_["state"], pool["u"][k], pool["delta"][k], L_["A"], pool["Bm"][k], pool["Cm"][k],
@@ -443,9 +474,9 @@ def run_decode(ssm, dev, hbm_peak, world, steps=None):
     state_bytes = cfg.batch * cfg.dim * cfg.dstate * 4
     per_call = 2 * state_bytes + 3 * cfg.batch * cfg.dim * 2 + 2 * cfg.batch * cfg.dstate * 2 + \
         cfg.batch * cfg.dim * 2 + cfg.dim * (cfg.dstate + 2) * 4
-    calls = steps * cfg.layers
+    calls = steps * nl
     gbs = per_call * calls / (ms * 1e-3) / 1e9
-    return {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} x {cfg.layers} layers "
+    return {"workload": f"{cfg.name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} x {nl} layers "
                         f"x {steps} tokens, bf16 I/O, fp32 state cache updated in place",
             "tokens_per_s": world * cfg.batch * steps / (ms * 1e-3), "ms_total": ms,
             "us_per_layer_call": ms * 1e3 / calls, "state_cache_gbs": 2 * state_bytes * calls / (ms * 1e-3) / 1e9,
@@ -500,6 +531,9 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of this kernel (reported as is)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="run only the decode workload")
+    ap.add_argument("--decode-layers", type=int, default=None, help="decode layers (default 64)")
+    ap.add_argument("--decode-steps", type=int, default=None, help="decode tokens (default 128)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-peaks", action="store_true", help="skip the bench_peaks.cu MUFU-rate probe")
