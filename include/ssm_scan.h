@@ -169,6 +169,17 @@ SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *del
                             int batch, int dim, int dstate, int delta_softplus, int zoh, ssm_dtype dtype,
                             ssm_stream_t stream);
 
+/*
+ * Device-side failures that a kernel could only record, not return.  (No counterpart on the pages.)
+ * The streamed decode kernel bounds every wait for its own bulk copies to about one second; on a
+ * timeout it sets a bit in a per-device flag, lets its copies still in flight land (again bounded) and
+ * returns, leaving the outputs of the affected tiles unwritten and the context usable.  This call
+ * synchronises the current device, stores the flag in *flags (0: nothing recorded; bit 0: a decode
+ * wait timed out) and clears it.
+ * Errors: SSM_ERR_INVALID_ARG (flags NULL), SSM_ERR_CUDA (the synchronisation or the read failed).
+ */
+SSM_API ssm_status ssm_device_error(unsigned *flags);
+
 /* Thread-local description of the most recent failed call on this thread ("" if none). */
 SSM_API const char *ssm_last_error(void);
 

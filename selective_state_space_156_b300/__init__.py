@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
         L.ssm_state_update.restype = st
         L.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        L.ssm_device_error.restype = st
+        L.ssm_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.ssm_last_error.restype = ctypes.c_char_p
         L.ssm_last_error.argtypes = []
         L.ssm_version.restype = ctypes.c_char_p
@@ -241,3 +243,11 @@ def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, 
                                   _ptr(y, "y", dt, (Bsz, D)), Bsz, D, N, int(bool(delta_softplus)), int(bool(zoh)),
                                   _DT[dt], _stream(stream)))
     return y
+
+
+def ssm_device_error() -> int:
+    """Synchronises the current device and returns (and clears) the flags that kernels record when a
+    bounded wait runs out: 0 when nothing was recorded, bit 0 for a decode-kernel wait."""
+    flags = ctypes.c_uint(0)
+    _check(lib().ssm_device_error(ctypes.byref(flags)))
+    return int(flags.value)

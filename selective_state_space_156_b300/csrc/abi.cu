@@ -206,6 +206,13 @@ const char* ssm_last_error(void) { return g_last_error.c_str(); }
 
 const char* ssm_version(void) { return "ssm_b300 0.1 (sm_103a)"; }
 
+ssm_status ssm_device_error(unsigned* flags) {
+    if (flags == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_device_error: flags is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: cudaDeviceSynchronize");
+    return cuda_status(ssm::take_bulk_wait_error(flags), "ssm_device_error: reading the flag");
+}
+
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     if (validate_scan(p) != SSM_OK) return 0;
     return workspace_bytes_for(p, plan_segments(scan_kind(p), choose_lpc(p), p->batch, p->dim, p->seqlen));

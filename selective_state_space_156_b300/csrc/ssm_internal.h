@@ -55,6 +55,17 @@ cudaError_t launch_state_update(float* state, const void* u, const void* delta, 
                                 const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
                                 int Bsz, int D, int N, int softplus, int zoh, int dtype, cudaStream_t stream);
 
+// The streamed decode kernel (state_update_bulk.cu): eligibility, launch, and the flag its bounded
+// waits set on a timeout (read and cleared by take_bulk_wait_error, which synchronises).
+bool state_update_bulk_eligible(const float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, int D,
+                                int N);
+cudaError_t launch_state_update_bulk(float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                                     const void* Cm, const float* Dskip, const float* delta_bias, const void* z,
+                                     void* y, int Bsz, int D, int N, int softplus, int zoh, int dtype,
+                                     cudaStream_t stream);
+cudaError_t take_bulk_wait_error(unsigned* flags);
+
 // Launch geometry of each kernel kind, used by the host to plan the L split.
 constexpr int kSeqChanPerBlock = 128, kSeqBlocksPerSM = 3, kSeqChunk = 64;
 constexpr int kG4ChanPerBlock = 32, kG4BlocksPerSM = 7, kG4ChunkSteps = 32;

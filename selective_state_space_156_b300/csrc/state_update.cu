@@ -4,6 +4,9 @@
 // cache shape (batch, d_inner, d_state) from lshu.cn/news/79586 section 6.5).
 // HBM-bound: the state is read and written once per call (2 * B * D * N * 4 bytes).
 // With N <= 16 each lane holds at most 4 states; N = 32 and 64 give 8 and 16 per lane.
+#include <cstdlib>
+#include <cstring>
+
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -173,9 +176,22 @@ static cudaError_t launch_su_t(float* state, const void* u, const void* delta, c
     return launch_su_ns<T, 32>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
 }
 
+// SSM_DECODE_KERNEL=rows keeps every call on the row kernel above (for comparisons); by default calls
+// that meet its requirements take the streamed kernel of state_update_bulk.cu.
+static bool bulk_decode_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("SSM_DECODE_KERNEL");
+        return !(v != nullptr && std::strcmp(v, "rows") == 0);
+    }();
+    return on;
+}
+
 cudaError_t launch_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
                                 const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
                                 int Bsz, int D, int N, int softplus_on, int zoh, int dtype, cudaStream_t stream) {
+    if (bulk_decode_enabled() && state_update_bulk_eligible(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, D, N))
+        return launch_state_update_bulk(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh,
+                                        dtype, stream);
     if (dtype == 1)
         return launch_su_t<BF16>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
     return launch_su_t<F32>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);

@@ -1,0 +1,300 @@
+// Single-token decode step, streamed: a persistent kernel that moves the fp32 state cache (B, D, N)
+// through shared memory in tiles of 64 (b, d) rows with 1-D bulk copies (the TMA engine) and a ring of
+// mbarrier-tracked stages, so that every SM keeps several tiles of loads in flight while it computes
+// and stores the previous one.  The step is the scan body with L = 1 (datadaily.news "State space
+// models vs Transformer: a practical guide", section on how state space models work: h = Abar h +
+// Bbar x_t, y_t = C h + D x_t; cache (batch, d_inner, d_state) per lshu.cn/news/79586 section 6.5).
+//
+// A tile holds 64 consecutive channels of one batch row: their states and rows of A (N fp32 each),
+// their u, delta, z, D skip and dt bias, and the batch row's B and C.  One producer warp issues the
+// copies of each tile once the four consumer warps have released its stage (an "empty" mbarrier per
+// stage, one arrival per warp); consumers wait on the stage's "full" mbarrier (the copies' byte
+// count), so no warp waits on another except through the ring.  Consumer thread t of the 128 owns the
+// four states 4 (t mod N/4) .. +3 of a row; a warp therefore reads and writes whole 512-byte runs of
+// the state.  The new state leaves with 16-byte streaming stores straight from registers; y leaves
+// from the first lane of each row.
+//
+// Requirements (the host checks them before choosing this kernel): N in {8, 16, 32, 64}, D % 8 == 0
+// (every tile's row count is a multiple of 8, so every copy is a multiple of 16 bytes) and 16-byte
+// aligned state, A, u, delta, z, B, C, D skip and dt bias.
+//
+// Each wait on a stage is bounded (about one second).  On a timeout the warp records it in a flag that
+// ssm_device_error reads and stops; before the block leaves, one thread waits (bounded) for the copies
+// it issued but did not consume.
+#include <algorithm>
+
+#include "bulk_copy.cuh"
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kBulkThreads = 128;
+constexpr int kTileRows = 64;
+
+__device__ unsigned int g_bulk_wait_error = 0;
+
+constexpr int round16(int x) { return (x + 15) & ~15; }
+
+template <typename T, int N>
+struct BulkLayout {
+    static constexpr int kE = T::kBytes;
+    static constexpr int kState = kTileRows * N * 4;
+    static constexpr int kScal = round16(kTileRows * kE);
+    static constexpr int kBC = round16(N * kE);
+    static constexpr int kOffState = 0;
+    static constexpr int kOffA = kOffState + kState;
+    static constexpr int kOffU = kOffA + kState;
+    static constexpr int kOffDt = kOffU + kScal;
+    static constexpr int kOffZ = kOffDt + kScal;
+    static constexpr int kOffB = kOffZ + kScal;
+    static constexpr int kOffC = kOffB + kBC;
+    static constexpr int kOffD = kOffC + kBC;
+    static constexpr int kOffBias = kOffD + kTileRows * 4;
+    static constexpr int kBytes = round16(kOffBias + kTileRows * 4);
+    static constexpr int kStages = N <= 32 ? 4 : 3;
+    static constexpr int kSmem = 128 + kStages * kBytes;  // barriers and counters first
+};
+
+struct DecodeArgs {
+    float* state;
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* Bm;
+    const void* Cm;
+    const float* Dskip;
+    const float* delta_bias;
+    const void* z;
+    void* y;
+    int Bsz, D, softplus;
+};
+
+template <typename T>
+__device__ __forceinline__ float smem_scalar(const unsigned char* base, int i) {
+    if constexpr (T::kBytes == 4) {
+        return reinterpret_cast<const float*>(base)[i];
+    } else {
+        return bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[i]);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void smem_vec4(const unsigned char* base, int i, float (&v)[4]) {
+    if constexpr (T::kBytes == 4) {
+        const float4 w = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+        v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + i);
+        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    }
+}
+
+template <typename T, int N, bool kZOH>
+__global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(const DecodeArgs a) {
+    using L = BulkLayout<T, N>;
+    constexpr int S = L::kStages;
+    constexpr int E = L::kE;
+    constexpr int TPR = N / 4;                  // threads per row
+    constexpr int RPP = kBulkThreads / TPR;     // rows per pass
+    constexpr int kWarps = kBulkThreads / 32;   // consumer warps
+    extern __shared__ __align__(128) unsigned char bulk_smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(bulk_smem);   // copies of a stage landed
+    uint64_t* empty = full + S;                                // every consumer warp is done with a stage
+    int* counts = reinterpret_cast<int*>(empty + S);           // [0] tiles issued, [1 + w] tiles consumed by warp w
+    unsigned char* stages = bulk_smem + 128;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int tiles_per_b = (a.D + kTileRows - 1) / kTileRows;
+    const int total = a.Bsz * tiles_per_b;
+    const int G = gridDim.x;
+    const int nlocal = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / G + 1 : 0;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // producer warp: one lane streams the block's tiles into the stage ring
+        if (lane == 0) {
+            int j = 0;
+            for (; j < nlocal; ++j) {
+                const int s = j % S;
+                if (j >= S && !mbar_wait_bounded(&empty[s], (unsigned)((j / S - 1) & 1))) {
+                    atomicOr(&g_bulk_wait_error, 1u);
+                    break;
+                }
+                const int t = (int)blockIdx.x + j * G;
+                const int b = t / tiles_per_b;
+                const int d0 = (t - b * tiles_per_b) * kTileRows;
+                const int rows = min(kTileRows, a.D - d0);
+                const size_t r0 = (size_t)b * a.D + d0;
+                uint64_t* bar = &full[s];
+                unsigned char* st = stages + s * L::kBytes;
+                const unsigned sb = (unsigned)(rows * N * 4), eb = (unsigned)(rows * E), pb = (unsigned)(rows * 4);
+                const unsigned bytes = 2 * sb + 2 * eb + (a.z ? eb : 0u) + 2u * N * E + (a.Dskip ? pb : 0u) +
+                                       (a.delta_bias ? pb : 0u);
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_g2s(st + L::kOffState, a.state + r0 * N, sb, bar);
+                bulk_g2s(st + L::kOffA, a.A + (size_t)d0 * N, sb, bar);
+                bulk_g2s(st + L::kOffU, static_cast<const unsigned char*>(a.u) + r0 * E, eb, bar);
+                bulk_g2s(st + L::kOffDt, static_cast<const unsigned char*>(a.delta) + r0 * E, eb, bar);
+                if (a.z) bulk_g2s(st + L::kOffZ, static_cast<const unsigned char*>(a.z) + r0 * E, eb, bar);
+                bulk_g2s(st + L::kOffB, static_cast<const unsigned char*>(a.Bm) + (size_t)b * N * E, N * E, bar);
+                bulk_g2s(st + L::kOffC, static_cast<const unsigned char*>(a.Cm) + (size_t)b * N * E, N * E, bar);
+                if (a.Dskip) bulk_g2s(st + L::kOffD, a.Dskip + d0, pb, bar);
+                if (a.delta_bias) bulk_g2s(st + L::kOffBias, a.delta_bias + d0, pb, bar);
+            }
+            counts[0] = j;
+        }
+    } else {
+        const int q = tid % TPR;
+        int j = 0;
+        for (; j < nlocal; ++j) {
+            const int s = j % S;
+            if (!mbar_wait_bounded(&full[s], (unsigned)((j / S) & 1))) {
+                if (lane == 0) atomicOr(&g_bulk_wait_error, 1u);
+                break;
+            }
+            const int t = (int)blockIdx.x + j * G;
+            const int b = t / tiles_per_b;
+            const int d0 = (t - b * tiles_per_b) * kTileRows;
+            const int rows = min(kTileRows, a.D - d0);
+            const size_t r0 = (size_t)b * a.D + d0;
+            const unsigned char* st = stages + s * L::kBytes;
+            const float* hs = reinterpret_cast<const float*>(st + L::kOffState);
+            const float* As = reinterpret_cast<const float*>(st + L::kOffA);
+            const float* Ds = reinterpret_cast<const float*>(st + L::kOffD);
+            const float* bs = reinterpret_cast<const float*>(st + L::kOffBias);
+            float Bv[4], Cv[4];
+            smem_vec4<T>(st + L::kOffB, 4 * q, Bv);
+            smem_vec4<T>(st + L::kOffC, 4 * q, Cv);
+#pragma unroll
+            for (int p = 0; p < kTileRows / RPP; ++p) {
+                // every lane takes part in the shuffles; rows past the tile's end compute on stale values
+                // and store nothing
+                const int r = p * RPP + tid / TPR;
+                const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + 4 * q);
+                const float4 av = *reinterpret_cast<const float4*>(As + r * N + 4 * q);
+                const float uv = smem_scalar<T>(st + L::kOffU, r);
+                const float sr = smem_scalar<T>(st + L::kOffDt, r) + (a.delta_bias ? bs[r] : 0.0f);
+                const float zr = a.z ? smem_scalar<T>(st + L::kOffZ, r) : 0.0f;
+                const float dsk = a.Dskip ? Ds[r] : 0.0f;
+                float dt, gate;
+                if constexpr (T::kBytes == 2) {  // bf16 I/O: the MUFU forms
+                    dt = a.softplus ? softplus_fast(sr) : sr;
+                    gate = a.z ? silu_fast(zr) : 1.0f;
+                } else {
+                    dt = a.softplus ? softplus(sr) : sr;
+                    gate = a.z ? silu(zr) : 1.0f;
+                }
+                float h[4] = {hv.x, hv.y, hv.z, hv.w};
+                const float A4[4] = {av.x, av.y, av.z, av.w};
+                const float dtu = dt * uv;
+                float yp = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float ab = ex2(dt * (A4[i] * kLog2e));
+                    if (kZOH) {
+                        // branch-free: the a -> 0 limit (Abar = 1, Bbar = dt B) is selected, not branched to
+                        const bool nz = A4[i] != 0.0f;
+                        const float ng = nz ? (uv * -rcp(A4[i])) * Bv[i] : 0.0f;
+                        const float hz = fmaf(ab, h[i] - ng, ng);
+                        h[i] = nz ? hz : fmaf(dtu, Bv[i], h[i]);
+                    } else {
+                        h[i] = fmaf(ab, h[i], dtu * Bv[i]);
+                    }
+                    yp = fmaf(Cv[i], h[i], yp);
+                }
+#pragma unroll
+                for (int m = 1; m < TPR; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
+                if (r < rows) {
+                    __stcs(reinterpret_cast<float4*>(a.state + (r0 + r) * N + 4 * q), make_float4(h[0], h[1], h[2], h[3]));
+                    if (q == 0) store1<T>(a.y, r0 + r, fmaf(dsk, uv, yp) * gate);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (lane == 0) counts[1 + warp] = j;
+    }
+
+    __syncthreads();
+    if (tid == 0) {
+        // after a timeout, let the copies this block issued but did not consume land before it leaves
+        int consumed = nlocal;
+        for (int w = 0; w < kWarps; ++w) consumed = min(consumed, counts[1 + w]);
+        for (int jj = consumed; jj < counts[0]; ++jj) mbar_wait_bounded(&full[jj % S], (unsigned)((jj / S) & 1));
+    }
+}
+
+template <typename T, int N, bool kZOH>
+cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
+    using L = BulkLayout<T, N>;
+    auto kfn = state_update_bulk_kernel<T, N, kZOH>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kBulkThreads + 32, L::kSmem)) != cudaSuccess) return e;
+    const long long tiles = (long long)a.Bsz * ((a.D + kTileRows - 1) / kTileRows);
+    const int grid = (int)std::min<long long>(tiles, (long long)sms * std::max(per_sm, 1));
+    kfn<<<grid, kBulkThreads + 32, L::kSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int N>
+cudaError_t launch_bulk_n(const DecodeArgs& a, int zoh, cudaStream_t s) {
+    return zoh ? launch_bulk<T, N, true>(a, s) : launch_bulk<T, N, false>(a, s);
+}
+
+template <typename T>
+cudaError_t launch_bulk_t(const DecodeArgs& a, int N, int zoh, cudaStream_t s) {
+    switch (N) {
+        case 8: return launch_bulk_n<T, 8>(a, zoh, s);
+        case 16: return launch_bulk_n<T, 16>(a, zoh, s);
+        case 32: return launch_bulk_n<T, 32>(a, zoh, s);
+        default: return launch_bulk_n<T, 64>(a, zoh, s);
+    }
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool state_update_bulk_eligible(const float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, int D,
+                                int N) {
+    if (N != 8 && N != 16 && N != 32 && N != 64) return false;
+    if (D % 8 != 0) return false;
+    return al16(state) && al16(u) && al16(delta) && al16(A) && al16(Bm) && al16(Cm) && (!Dskip || al16(Dskip)) &&
+           (!delta_bias || al16(delta_bias)) && (!z || al16(z));
+}
+
+cudaError_t launch_state_update_bulk(float* state, const void* u, const void* delta, const float* A, const void* Bm,
+                                     const void* Cm, const float* Dskip, const float* delta_bias, const void* z,
+                                     void* y, int Bsz, int D, int N, int softplus_on, int zoh, int dtype,
+                                     cudaStream_t stream) {
+    const DecodeArgs a{state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, softplus_on};
+    if (dtype == 1) return launch_bulk_t<BF16>(a, N, zoh, stream);
+    return launch_bulk_t<F32>(a, N, zoh, stream);
+}
+
+cudaError_t take_bulk_wait_error(unsigned* flags) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_bulk_wait_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_bulk_wait_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace ssm

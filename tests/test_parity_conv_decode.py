@@ -91,6 +91,41 @@ def test_state_update(N, dtype, zoh):
     assert_close(st, st_ref, h_tolerance(st_ref, torch.float32), "state")
 
 
+@pytest.mark.parametrize("N", [8, 16, 32, 64])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(2, 8), (5, 200), (128, 3584)])
+def test_state_update_streamed(N, dtype, shape):
+    """The streamed (bulk-copy) decode kernel: D % 8 == 0 and aligned tensors.  (5, 200) ends every batch
+    row with a partial tile of 8 rows; (128, 3584) gives every block more tiles than its stage ring holds,
+    so the ring wraps several times."""
+    Bsz, D = shape
+    s = _step_inputs(Bsz, D, N, dtype, 1000 + N + D)
+    g = to_dev(s)
+    st = g["state"].clone()
+    y = Guarded((Bsz, D), dtype)
+    ssm.ssm_state_update(st, g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], Dskip=g["Dskip"],
+                         delta_bias=g["delta_bias"], z=g["z"], y=y.t)
+    assert ssm.ssm_device_error() == 0
+    y.check_bands()
+    st_ref, y_ref = oracle.state_update(s["state"], s["u"], s["delta"], s["A"], s["Bm"], s["Cm"], s["Dskip"],
+                                        s["delta_bias"], s["z"])
+    assert_close(y.t, y_ref, y_tolerance(y_ref, dtype), "y")
+    assert_close(st, st_ref, h_tolerance(st_ref, torch.float32), "state")
+
+
+def test_state_update_streamed_without_optional_inputs_and_zero_A():
+    s = _step_inputs(4, 128, 16, torch.bfloat16, 17, with_z=False, with_D=False)
+    s["A"][70, 5] = 0.0
+    s["delta_bias"] = None
+    g = to_dev(s)
+    st = g["state"].clone()
+    y = ssm.ssm_state_update(st, g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], zoh=True)
+    assert ssm.ssm_device_error() == 0
+    st_ref, y_ref = oracle.state_update(s["state"], s["u"], s["delta"], s["A"], s["Bm"], s["Cm"])
+    assert_close(y, y_ref, y_tolerance(y_ref, torch.bfloat16), "y")
+    assert_close(st, st_ref, h_tolerance(st_ref, torch.float32), "state")
+
+
 def test_state_update_optional_inputs_and_zero_A():
     s = _step_inputs(2, 64, 16, torch.float32, 5, with_z=False, with_D=False)
     s["A"][7, 3] = 0.0
