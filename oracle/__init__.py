@@ -42,15 +42,15 @@ def _load():
         lib = ctypes.CDLL(build())
         lib.oracle_scan_rows.restype = ctypes.c_int
         lib.oracle_scan_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, _ip,
-                                         _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int,
+                                         _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, _dp, _dp,
                                          _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_conv1d_rows.restype = ctypes.c_int
         lib.oracle_conv1d_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, _dp, _dp, _dp,
                                            ctypes.c_int, _dp]
         lib.oracle_state_update.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
-                                            _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_int]
+                                            _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, _dp, _dp,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -77,11 +77,13 @@ def _iptr(a: np.ndarray):
 
 
 def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0, zoh: Optional[bool] = None,
-         delta_softplus: Optional[bool] = None):
+         delta_softplus: Optional[bool] = None, extra: Optional[dict] = None):
     """Selective scan of a workload dict (see ``workloads.make_scan_inputs``).
 
     ``rows``: optional list of (b, d) pairs to compute; default is every row in (b, d) order.
-    Returns (y (R, L), h_out (R, N), threads_used) as fp64 numpy arrays.
+    ``inputs["conv_init"]`` (B, D, W-1), when present with a conv, is the x history before t = 0.
+    Returns (y (R, L), h_out (R, N), threads_used) as fp64 numpy arrays; with a dict ``extra`` and a
+    conv, also stores the last W-1 inputs of every row as ``extra["conv_final"]`` (R, W-1).
     """
     lib = _load()
     Bsz, D, L = tuple(inputs["u"].shape)
@@ -121,15 +123,19 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
     W = 0 if cw is None else cw.shape[1]
     if cw is not None and cb is None:
         cb = np.zeros(D)
+    ci = rows_of(inputs.get("conv_init"), W - 1) if (cw is not None and W > 1) else None
+    cf = np.zeros((R, max(W - 1, 1)), dtype=np.float64) if (cw is not None and extra is not None) else None
     y = np.empty((R, L), dtype=np.float64)
     h_out = np.empty((R, N), dtype=np.float64)
     z_flag = inputs.get("zoh", True) if zoh is None else zoh
     sp_flag = inputs.get("delta_softplus", True) if delta_softplus is None else delta_softplus
     nt = lib.oracle_scan_rows(R, L, N, _iptr(rb), _iptr(rd), _ptr(ur), _ptr(dr), _ptr(zr), _ptr(A), _ptr(Dskip),
-                              _ptr(bias), _ptr(cw), _ptr(cb), W, _ptr(Bm), _ptr(Cm), _ptr(h0), _ptr(y),
-                              _ptr(h_out), int(bool(sp_flag)), int(bool(z_flag)), int(nthreads))
+                              _ptr(bias), _ptr(cw), _ptr(cb), W, _ptr(ci), _ptr(cf), _ptr(Bm), _ptr(Cm), _ptr(h0),
+                              _ptr(y), _ptr(h_out), int(bool(sp_flag)), int(bool(z_flag)), int(nthreads))
     if nt < 0:
         raise ValueError("oracle_scan_rows rejected its arguments")
+    if cf is not None:
+        extra["conv_final"] = cf[:, :W - 1]
     return y, h_out, nt
 
 
@@ -160,18 +166,28 @@ def conv1d(x, w, b=None, silu: bool = True, rows: Optional[Sequence[tuple]] = No
 
 
 def state_update(state, u, delta, A, Bm, Cm, Dskip=None, delta_bias=None, z=None, zoh: bool = True,
-                 delta_softplus: bool = True, nthreads: int = 0):
+                 delta_softplus: bool = True, nthreads: int = 0, conv_w=None, conv_b=None, conv_state=None):
     """One decode step.  ``state`` (B, D, N) is widened to fp64 and returned updated (not in place)
-    together with y (B, D)."""
+    together with y (B, D).  With ``conv_w`` (D, W), u is the conv input x and ``conv_state``
+    (B, D, W-1) the previous W-1 inputs; the updated conv state is returned third."""
     lib = _load()
     st = f64(state).copy()
     ua = f64(u)
     Bsz, D = ua.shape
     N = st.shape[2]
     y = np.empty((Bsz, D), dtype=np.float64)
+    cw = f64(conv_w)
+    W = 0 if cw is None else cw.shape[1]
+    cs = None
+    if cw is not None:
+        cs = (f64(conv_state).copy() if conv_state is not None and W > 1
+              else np.zeros((Bsz, D, max(W - 1, 1)), dtype=np.float64))
     rc = lib.oracle_state_update(Bsz, D, N, _ptr(st), _ptr(ua), _ptr(f64(delta)), _ptr(f64(A)), _ptr(f64(Bm)),
-                                 _ptr(f64(Cm)), _ptr(f64(Dskip)), _ptr(f64(delta_bias)), _ptr(f64(z)), _ptr(y),
-                                 int(bool(delta_softplus)), int(bool(zoh)), int(nthreads))
+                                 _ptr(f64(Cm)), _ptr(f64(Dskip)), _ptr(f64(delta_bias)), _ptr(f64(z)), _ptr(cw),
+                                 _ptr(f64(conv_b)), W, _ptr(cs), _ptr(y), int(bool(delta_softplus)), int(bool(zoh)),
+                                 int(nthreads))
     if rc < 0:
         raise ValueError("oracle_state_update rejected its arguments")
+    if cw is not None:
+        return st, y, cs[..., :W - 1]
     return st, y

@@ -49,6 +49,8 @@ typedef struct {
     const double *conv_w, *conv_b;        /* (D, W), (D) or NULL                   */
     const double *Bm, *Cm;                /* (batch, N, L), indexed by row's batch */
     const double *h0;                     /* (R, N) or NULL                        */
+    const double *conv_init;              /* (R, W-1): x before t = 0, or NULL     */
+    double *conv_final;                   /* (R, W-1): the last W-1 x, or NULL     */
     double *y, *h_out;                    /* (R, L), (R, N) or NULL                */
     int delta_softplus, zoh;
     int next_row;                         /* work counter, guarded by lock         */
@@ -64,18 +66,31 @@ static void scan_one_row(const scan_job *j, int r, double *h, double *v) {
     const double *Bb = j->Bm + (size_t)b * N * L;
     const double *Cb = j->Cm + (size_t)b * N * L;
 
-    /* Input to the SSM: the raw u, or SiLU(causal depthwise conv of x) when a conv is given. */
+    /* Input to the SSM: the raw u, or SiLU(causal depthwise conv of x) when a conv is given.
+       x before t = 0 is the row's conv_init history (oldest first) when given, else zero. */
+    const double *xi = j->conv_init ? j->conv_init + (size_t)r * (W - 1) : NULL;
     for (int t = 0; t < L; ++t) {
         if (j->conv_w) {
             double acc = j->conv_b ? j->conv_b[d] : 0.0;
             for (int k = 0; k < W; ++k) {
                 int src = t - (W - 1) + k;        /* tap k = W-1 multiplies x_t, tap 0 multiplies x_{t-W+1} */
                 if (src >= 0) acc += j->conv_w[(size_t)d * W + k] * ur[src];
+                else if (xi) acc += j->conv_w[(size_t)d * W + k] * xi[(W - 1) + src];
             }
             v[t] = silu(acc);
         } else {
             v[t] = ur[t];
         }
+    }
+    /* The conv history the next call needs: x_{L-W+1} .. x_{L-1}, reaching back into conv_init when
+       L < W - 1.  Staged first: conv_final may be the same buffer as conv_init. */
+    if (j->conv_w && j->conv_final && W > 1) {
+        double hist[8];
+        for (int i = 0; i < W - 1; ++i) {
+            int t = L - (W - 1) + i;
+            hist[i] = t >= 0 ? ur[t] : (xi ? xi[(W - 1) + t] : 0.0);
+        }
+        for (int i = 0; i < W - 1; ++i) j->conv_final[(size_t)r * (W - 1) + i] = hist[i];
     }
 
     for (int n = 0; n < N; ++n) h[n] = j->h0 ? j->h0[(size_t)r * N + n] : 0.0;
@@ -140,16 +155,19 @@ ORACLE_API int oracle_scan_rows(int R, int L, int N, const int *row_b, const int
                                 const double *u, const double *delta, const double *z,
                                 const double *A, const double *Dskip, const double *delta_bias,
                                 const double *conv_w, const double *conv_b, int conv_width,
+                                const double *conv_init, double *conv_final,
                                 const double *Bm, const double *Cm, const double *h0,
                                 double *y, double *h_out, int delta_softplus, int zoh, int nthreads) {
     if (R < 0 || L < 0 || N <= 0 || !row_b || !row_d || !u || !delta || !A || !Bm || !Cm || !y) return -1;
-    if (conv_w && conv_width <= 0) return -1;
+    if (conv_w && (conv_width <= 0 || conv_width > 8)) return -1;
     scan_job j;
     memset(&j, 0, sizeof(j));
     j.R = R; j.L = L; j.N = N; j.W = conv_width;
     j.row_b = row_b; j.row_d = row_d;
     j.u = u; j.delta = delta; j.z = z; j.A = A; j.Dskip = Dskip; j.delta_bias = delta_bias;
     j.conv_w = conv_w; j.conv_b = conv_b; j.Bm = Bm; j.Cm = Cm; j.h0 = h0; j.y = y; j.h_out = h_out;
+    j.conv_init = conv_w ? conv_init : NULL;
+    j.conv_final = conv_w ? conv_final : NULL;
     j.delta_softplus = delta_softplus; j.zoh = zoh;
     pthread_mutex_init(&j.lock, NULL);
     int nt = resolve_threads(nthreads, R);
@@ -186,11 +204,17 @@ ORACLE_API int oracle_conv1d_rows(int R, int L, int W, const int *row_d, const d
 /*
  * Single-token state update: the scan body with L = 1, starting from state (B, D, N)
  * and writing it back in place.  u, delta, z, y are (B, D); Bm, Cm are (B, N).
+ * With conv_w given, u is the conv input x and conv_state (B, D, W-1) holds the previous W-1
+ * inputs (oldest first): the step reads it as the conv history and leaves the last W-1 inputs
+ * there (the decode cache's conv part: dpshk.com/news/5205047 section 1.3, lshu.cn/news/79586
+ * section 6.5).
  */
 ORACLE_API int oracle_state_update(int Bsz, int D, int N, double *state, const double *u, const double *delta,
                                    const double *A, const double *Bm, const double *Cm, const double *Dskip,
-                                   const double *delta_bias, const double *z, double *y, int delta_softplus,
-                                   int zoh, int nthreads) {
+                                   const double *delta_bias, const double *z, const double *conv_w,
+                                   const double *conv_b, int conv_width, double *conv_state, double *y,
+                                   int delta_softplus, int zoh, int nthreads) {
+    if (conv_w && !conv_state && conv_width > 1) return -1;
     if (Bsz < 0 || D < 0 || N <= 0 || !state || !u || !delta || !A || !Bm || !Cm || !y) return -1;
     int R = Bsz * D;
     int *rb = (int *)malloc(sizeof(int) * (size_t)(R > 0 ? R : 1));
@@ -200,8 +224,8 @@ ORACLE_API int oracle_state_update(int Bsz, int D, int N, double *state, const d
     /* With L = 1 the (B, N, L) layout of Bm/Cm is exactly the (B, N) layout given here, and the
        state (B, D, N) is the compact (R, N) layout; scan_one_row copies h0 before it writes h_out,
        so passing the same buffer for both is safe. */
-    int rc = oracle_scan_rows(R, 1, N, rb, rd, u, delta, z, A, Dskip, delta_bias, NULL, NULL, 0, Bm, Cm,
-                              state, y, state, delta_softplus, zoh, nthreads);
+    int rc = oracle_scan_rows(R, 1, N, rb, rd, u, delta, z, A, Dskip, delta_bias, conv_w, conv_b, conv_width,
+                              conv_state, conv_state, Bm, Cm, state, y, state, delta_softplus, zoh, nthreads);
     free(rb);
     free(rd);
     return rc;

@@ -330,6 +330,76 @@ def test_p9_conv_front_end_matches_library_conv1d():
 
 
 # ---------------------------------------------------------------------------------------------
+# P12: conv history carried across calls.  With conv_init (the W-1 inputs before t = 0) the front end
+# equals torch's conv1d over the history and x concatenated; conv_final returns the last W-1 inputs;
+# and a split run that passes conv_final and h_out on equals one run (dpshk.com/news/5205047 1.3,
+# pwwt.cn/news/5168881 3.1: the carried state of a chunked prefill)
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("W", [2, 3, 4])
+def test_p12_conv_history_matches_library_conv1d(W):
+    d = _inputs(2, 5, 4, 19, conv=True, seed=12 + W)
+    d["conv_w"] = d["conv_w"][:, :W].contiguous()
+    g = np.random.default_rng(40 + W)
+    hist = torch.tensor(g.standard_normal((2, 5, W - 1)))
+    d["conv_init"] = hist
+    full = torch.cat([hist, d["u"]], dim=-1)
+    ref = torch.nn.functional.conv1d(full, d["conv_w"][:, None, :], d["conv_b"], groups=5)  # valid: length L
+    assert ref.shape[-1] == 19
+    extra = {}
+    y_fused, h_fused, _ = oracle.scan(d, extra=extra)
+    d2 = dict(d, conv_w=None, conv_b=None, conv_init=None, u=torch.tensor(_silu_torch(ref.numpy())))
+    y_plain, h_plain, _ = oracle.scan(d2)
+    np.testing.assert_allclose(y_fused, y_plain, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(h_fused, h_plain, rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(extra["conv_final"], full[..., -(W - 1):].reshape(10, W - 1).numpy())
+
+
+@pytest.mark.parametrize("L1", [1, 2, 3, 7, 16])
+def test_p12_split_with_conv_history_equals_one_run(L1):
+    L = 23
+    d = _inputs(2, 3, 4, L, conv=True, with_z=True, h0=True, seed=120 + L1)
+    y, h, _ = oracle.scan(d)
+    first = dict(d, u=d["u"][..., :L1], delta=d["delta"][..., :L1], z=d["z"][..., :L1], Bm=d["Bm"][..., :L1],
+                 Cm=d["Cm"][..., :L1])
+    e1 = {}
+    y1, h1, _ = oracle.scan(first, extra=e1)
+    second = dict(d, u=d["u"][..., L1:], delta=d["delta"][..., L1:], z=d["z"][..., L1:], Bm=d["Bm"][..., L1:],
+                  Cm=d["Cm"][..., L1:], h0=torch.tensor(h1.reshape(2, 3, 4)),
+                  conv_init=torch.tensor(e1["conv_final"].reshape(2, 3, 3)))
+    e2 = {}
+    y2, h2, _ = oracle.scan(second, extra=e2)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=1), y, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(h2, h, rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(e2["conv_final"], d["u"][..., -3:].reshape(6, 3).numpy())
+
+
+# ---------------------------------------------------------------------------------------------
+# P13: decode with a conv state: L single-token steps that carry (conv state, SSM state) equal one
+# fused scan of length L (datadaily.news "State space models vs Transformer: a practical guide";
+# lshu.cn/news/79586 6.5: the cache holds the conv and the SSM state)
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_p13_decode_with_conv_state_equals_fused_scan(W):
+    L = 12
+    d = _inputs(2, 3, 4, L, conv=True, with_z=True, h0=True, seed=130 + W)
+    d["conv_w"] = d["conv_w"][:, :W].contiguous()
+    y, h, _ = oracle.scan(d)
+    st = d["h0"].clone()
+    cs = torch.zeros((2, 3, max(W - 1, 1)), dtype=torch.float64)[..., :W - 1]
+    ys = []
+    for t in range(L):
+        st_np, yt, cs_np = oracle.state_update(st, d["u"][..., t], d["delta"][..., t], d["A"], d["Bm"][..., t],
+                                               d["Cm"][..., t], d["Dskip"], d["delta_bias"], d["z"][..., t],
+                                               conv_w=d["conv_w"], conv_b=d["conv_b"], conv_state=cs)
+        st, cs = torch.tensor(st_np), torch.tensor(np.ascontiguousarray(cs_np))
+        ys.append(yt)
+    np.testing.assert_allclose(np.stack(ys, axis=-1).reshape(6, L), y, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(st.numpy().reshape(6, 4), h, rtol=1e-13, atol=1e-14)
+    if W > 1:
+        np.testing.assert_array_equal(cs.numpy(), d["u"][..., -(W - 1):].numpy())
+
+
+# ---------------------------------------------------------------------------------------------
 # P10: N = 1, no D, simplified Bbar: scalar closed form y_k = c_k sum_i (prod_{j=i+1..k} a_j) b_i x_i
 # ---------------------------------------------------------------------------------------------
 def test_p10_scalar_closed_form():
