@@ -92,6 +92,14 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  *                   B * D alone cannot fill the GPU.  NULL / too small is not an error: the call
  *                   then runs without the split.  Size it with ssm_scan_workspace_size().  The
  *                   workspace must not be shared by calls that may run concurrently.
+ *   conv_init   (B, D, conv_width-1) in_dtype   the conv inputs x_{-W+1} .. x_{-1} (oldest first)
+ *                   that precede this call's x, or NULL for zeros: the history a chunked prefill
+ *                   carries from one call to the next.  Ignored without conv_w.
+ *   conv_final  (B, D, conv_width-1) in_dtype   receives the last conv_width-1 inputs of the
+ *                   sequence (reaching back into conv_init when seqlen < conv_width-1), ready to be
+ *                   the next call's conv_init or the decode conv state; NULL if not wanted.  May be
+ *                   the same buffer as conv_init; must not overlap any other tensor.  Ignored
+ *                   without conv_w.
  */
 typedef struct ssm_scan_params {
     int batch, dim, dstate, seqlen;
@@ -114,6 +122,8 @@ typedef struct ssm_scan_params {
     int zoh;
     void *workspace;
     size_t workspace_bytes;
+    const void *conv_init;
+    void *conv_final;
 } ssm_scan_params;
 
 /* Selective scan forward (with the optional fused conv front end, D skip and gate).
@@ -179,6 +189,46 @@ SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *del
  * Errors: SSM_ERR_INVALID_ARG (flags NULL), SSM_ERR_CUDA (the synchronisation or the read failed).
  */
 SSM_API ssm_status ssm_device_error(unsigned *flags);
+
+/*
+ * Single-token decode step with the conv front end fused: the decode cache holds a conv state and
+ * the SSM state (dpshk.com/news/5205047 section 1.3; lshu.cn/news/79586 section 6.5).  Per (b, d):
+ *   v   = SiLU(conv_b[d] + sum_{k<W-1} conv_w[d,k] conv_state[b,d,k] + conv_w[d,W-1] x[b,d])
+ *   conv_state[b,d,:] <- (conv_state[b,d,1:], x[b,d])        (the last W-1 inputs, oldest first)
+ * then the step of ssm_state_update with v as its input.  With conv_w == NULL this is exactly
+ * ssm_state_update (x is u; conv_state is ignored).
+ *
+ *   x           (B, D)    dtype      conv input (u when conv_w is NULL)            required
+ *   delta, z, y, Bm, Cm, A, Dskip, delta_bias, state: as in ssm_state_update
+ *   conv_w      (D, conv_width) f32  taps, tap conv_width-1 multiplies x; or NULL
+ *   conv_b      (D)       float32    conv bias or NULL (zero)
+ *   conv_width  int                  1..4 when conv_w != NULL
+ *   conv_state  (B, D, conv_width-1) dtype, read and written in place; required when
+ *                                    conv_width > 1; must not overlap any other tensor
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED (dstate), SSM_ERR_CUDA.
+ */
+typedef struct ssm_step_params {
+    int batch, dim, dstate;
+    ssm_dtype dtype;
+    float *state;
+    const void *x;
+    const void *delta;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *Dskip;
+    const float *delta_bias;
+    const void *z;
+    const float *conv_w;
+    const float *conv_b;
+    int conv_width;
+    void *conv_state;
+    void *y;
+    int delta_softplus;
+    int zoh;
+} ssm_step_params;
+
+SSM_API ssm_status ssm_state_update_conv(const ssm_step_params *p, ssm_stream_t stream);
 
 /* Thread-local description of the most recent failed call on this thread ("" if none). */
 SSM_API const char *ssm_last_error(void);

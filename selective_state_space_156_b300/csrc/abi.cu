@@ -157,6 +157,53 @@ ssm_status validate_scan(const ssm_scan_params* p) {
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: y overlaps an input");
     if (p->h_out != nullptr && overlaps(p->h_out, rows * p->dstate * 4, p->y, ybytes))
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_out overlaps y");
+    if (p->conv_w != nullptr && p->conv_width > 1) {
+        const size_t cbytes = rows * (size_t)(p->conv_width - 1) * ib;
+        if (p->conv_init != nullptr && (overlaps(p->conv_init, cbytes, p->y, ybytes) ||
+                                        (p->h_out && overlaps(p->conv_init, cbytes, p->h_out, rows * p->dstate * 4))))
+            return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: conv_init overlaps an output");
+        if (p->conv_final != nullptr) {
+            const void* f = p->conv_final;
+            if (overlaps(f, cbytes, p->u, nbdl * ib) || overlaps(f, cbytes, p->delta, nbdl * ib) ||
+                overlaps(f, cbytes, p->z, nbdl * ib) || overlaps(f, cbytes, p->Bm, nbnl * ib) ||
+                overlaps(f, cbytes, p->Cm, nbnl * ib) || overlaps(f, cbytes, p->y, ybytes) ||
+                (p->h_out && overlaps(f, cbytes, p->h_out, rows * p->dstate * 4)) ||
+                (p->h0 && overlaps(f, cbytes, p->h0, rows * p->dstate * 4)) ||
+                (p->conv_init && p->conv_init != f && overlaps(f, cbytes, p->conv_init, cbytes)))
+                return fail(SSM_ERR_INVALID_ARG,
+                            "ssm_scan_fwd: conv_final overlaps another tensor (it may only be conv_init itself)");
+        }
+    }
+    return SSM_OK;
+}
+
+// The kernel arguments every scan entry point derives from the parameters the same way.
+ssm::ScanKernelArgs scan_args(const ssm_scan_params* p) {
+    ssm::ScanKernelArgs a{};
+    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
+    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm;
+    a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
+    a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
+    a.conv_init = (p->conv_w && p->conv_width > 1) ? p->conv_init : nullptr;
+    a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
+    a.softplus = p->delta_softplus;
+    a.vec = aligned_rows(p);
+    a.kind = scan_kind(p);
+    a.lpc = choose_lpc(p);
+    return a;
+}
+
+// The scan launches, then (when asked) the conv-history copy, which runs after the scan so that a
+// conv_final aliasing conv_init is only written once every block has read its history.
+ssm_status launch_scan_and_history(const ssm::ScanKernelArgs& a, const ssm_scan_params* p, ssm_stream_t stream,
+                                   const char* who) {
+    cudaError_t e = ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    if (p->conv_w != nullptr && p->conv_width > 1 && p->conv_final != nullptr) {
+        e = ssm::launch_conv_history(p->u, a.conv_init, p->conv_final, (size_t)p->batch * p->dim, p->seqlen,
+                                     p->conv_width - 1, (int)p->in_dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_status(e, who);
+    }
     return SSM_OK;
 }
 
@@ -222,16 +269,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
     ssm_status st = validate_scan(p);
     if (st != SSM_OK) return st;
 
-    ssm::ScanKernelArgs a{};
-    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
-    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm;
-    a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
-    a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
-    a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
-    a.softplus = p->delta_softplus;
-    a.vec = aligned_rows(p);
-    a.kind = scan_kind(p);
-    a.lpc = choose_lpc(p);
+    ssm::ScanKernelArgs a = scan_args(p);
 
     SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
     const size_t need = workspace_bytes_for(p, sp);
@@ -249,8 +287,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
         a.ws_h = w + (size_t)(sp.nseg - 1) * rows;
         a.ws_h0 = p->h0 != nullptr ? a.ws_h + (size_t)(sp.nseg - 1) * rows * p->dstate : nullptr;
     }
-    return cuda_status(ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream),
-                       "ssm_scan_fwd launch");
+    return launch_scan_and_history(a, p, stream, "ssm_scan_fwd launch");
 }
 
 ssm_status causal_conv1d_fwd(const void* x, const float* w, const float* b, void* y, int batch, int dim, int seqlen,
@@ -269,44 +306,87 @@ ssm_status causal_conv1d_fwd(const void* x, const float* w, const float* b, void
                        "causal_conv1d_fwd launch");
 }
 
+}  // extern "C"
+
+namespace {
+
+// Host-side checks and launch of one decode step (ssm_state_update and ssm_state_update_conv).
+ssm_status run_decode_step(const ssm::DecodeStep& st, ssm_dtype dtype, const char* who, cudaStream_t stream) {
+    if (!st.state || !st.x || !st.delta || !st.A || !st.Bm || !st.Cm || !st.y)
+        return fail(SSM_ERR_INVALID_ARG, "%s: state, x (u), delta, A, Bm, Cm and y are required", who);
+    if (st.Bsz <= 0 || st.D <= 0 || st.N <= 0) return fail(SSM_ERR_INVALID_ARG, "%s: sizes must be positive", who);
+    if (st.Bsz > 65535) return fail(SSM_ERR_UNSUPPORTED, "%s: batch %d exceeds 65535", who, st.Bsz);
+    if (!(st.N <= 16 || st.N == 32 || st.N == 64))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: dstate %d not supported (1..16, 32, 64)", who, st.N);
+    if ((st.softplus != 0 && st.softplus != 1) || (st.zoh != 0 && st.zoh != 1))
+        return fail(SSM_ERR_INVALID_ARG, "%s: delta_softplus and zoh must be 0 or 1", who);
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (st.conv_w != nullptr) {
+        if (st.conv_width < 1 || st.conv_width > 4)
+            return fail(SSM_ERR_INVALID_ARG, "%s: conv_width %d outside 1..4", who, st.conv_width);
+        if (st.conv_width > 1 && st.conv_state == nullptr)
+            return fail(SSM_ERR_INVALID_ARG, "%s: conv_state is required when conv_width > 1", who);
+    }
+    const size_t bd = (size_t)st.Bsz * st.D * esize(dtype);
+    const size_t bn = (size_t)st.Bsz * st.N * esize(dtype);
+    const size_t sb = (size_t)st.Bsz * st.D * st.N * 4;
+    const void* y = st.y;
+    if (overlaps(y, bd, st.x, bd) || overlaps(y, bd, st.delta, bd) || overlaps(y, bd, st.z, bd) ||
+        overlaps(y, bd, st.Bm, bn) || overlaps(y, bd, st.Cm, bn) || overlaps(y, bd, st.state, sb))
+        return fail(SSM_ERR_INVALID_ARG, "%s: y overlaps an input or the state", who);
+    if (st.conv_w != nullptr && st.conv_width > 1) {
+        const size_t cb = (size_t)st.Bsz * st.D * (st.conv_width - 1) * esize(dtype);
+        const void* c = st.conv_state;
+        if (overlaps(c, cb, st.x, bd) || overlaps(c, cb, st.delta, bd) || overlaps(c, cb, st.z, bd) ||
+            overlaps(c, cb, st.Bm, bn) || overlaps(c, cb, st.Cm, bn) || overlaps(c, cb, st.state, sb) ||
+            overlaps(c, cb, y, bd))
+            return fail(SSM_ERR_INVALID_ARG, "%s: conv_state overlaps another tensor", who);
+    }
+    return cuda_status(ssm::launch_state_update(st, stream), who);
+}
+
+ssm::DecodeStep decode_step(float* state, const void* x, const void* delta, const float* A, const void* Bm,
+                            const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
+                            int batch, int dim, int dstate, int delta_softplus, int zoh, ssm_dtype dtype) {
+    ssm::DecodeStep st{};
+    st.state = state; st.x = x; st.delta = delta; st.A = A; st.Bm = Bm; st.Cm = Cm;
+    st.Dskip = Dskip; st.delta_bias = delta_bias; st.z = z; st.y = y;
+    st.Bsz = batch; st.D = dim; st.N = dstate; st.softplus = delta_softplus; st.zoh = zoh; st.dtype = (int)dtype;
+    st.conv_width = 1;
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
 ssm_status ssm_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
                             const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
                             int batch, int dim, int dstate, int delta_softplus, int zoh, ssm_dtype dtype,
                             ssm_stream_t stream) {
-    if (!state || !u || !delta || !A || !Bm || !Cm || !y)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: state, u, delta, A, Bm, Cm and y are required");
-    if (batch <= 0 || dim <= 0 || dstate <= 0)
-        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: sizes must be positive");
-    if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "ssm_state_update: batch %d exceeds 65535", batch);
-    if (!(dstate <= 16 || dstate == 32 || dstate == 64))
-        return fail(SSM_ERR_UNSUPPORTED, "ssm_state_update: dstate %d not supported (1..16, 32, 64)", dstate);
-    if ((delta_softplus != 0 && delta_softplus != 1) || (zoh != 0 && zoh != 1))
-        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: delta_softplus and zoh must be 0 or 1");
-    if (dtype != SSM_F32 && dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: bad dtype");
-    const size_t bd = (size_t)batch * dim * esize(dtype);
-    const size_t bn = (size_t)batch * dstate * esize(dtype);
-    if (overlaps(y, bd, u, bd) || overlaps(y, bd, delta, bd) || overlaps(y, bd, z, bd) || overlaps(y, bd, Bm, bn) ||
-        overlaps(y, bd, Cm, bn) || overlaps(y, bd, state, (size_t)batch * dim * dstate * 4))
-        return fail(SSM_ERR_INVALID_ARG, "ssm_state_update: y overlaps an input or the state");
-    return cuda_status(ssm::launch_state_update(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, batch, dim, dstate,
-                                                delta_softplus, zoh, (int)dtype, (cudaStream_t)stream),
-                       "ssm_state_update launch");
+    const ssm::DecodeStep st = decode_step(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, batch, dim, dstate,
+                                           delta_softplus, zoh, dtype);
+    return run_decode_step(st, dtype, "ssm_state_update", (cudaStream_t)stream);
+}
+
+ssm_status ssm_state_update_conv(const ssm_step_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_state_update_conv: params is NULL");
+    ssm::DecodeStep st = decode_step(p->state, p->x, p->delta, p->A, p->Bm, p->Cm, p->Dskip, p->delta_bias, p->z,
+                                     p->y, p->batch, p->dim, p->dstate, p->delta_softplus, p->zoh, p->dtype);
+    if (p->conv_w != nullptr) {
+        st.conv_w = p->conv_w;
+        st.conv_b = p->conv_b;
+        st.conv_width = p->conv_width;
+        st.conv_state = p->conv_width > 1 ? p->conv_state : nullptr;
+    }
+    return run_decode_step(st, p->dtype, "ssm_state_update_conv", (cudaStream_t)stream);
 }
 
 ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
     ssm_status st = validate_scan(p);
     if (st != SSM_OK) return st;
 
-    ssm::ScanKernelArgs a{};
-    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
-    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm;
-    a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
-    a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
-    a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
-    a.softplus = p->delta_softplus;
-    a.vec = aligned_rows(p);
-    a.kind = scan_kind(p);
-    a.lpc = choose_lpc(p);
+    ssm::ScanKernelArgs a = scan_args(p);
 
     // the same launch plan as ssm_scan_fwd with a large enough workspace; p->workspace is ignored
     const SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
@@ -330,8 +410,7 @@ ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
         a.ws_h = w + (size_t)(sp.nseg - 1) * rows;
         a.ws_h0 = p->h0 != nullptr ? a.ws_h + (size_t)(sp.nseg - 1) * rows * p->dstate : nullptr;
     }
-    return cuda_status(ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream),
-                       "ssm_scan_fwd_static launch");
+    return launch_scan_and_history(a, p, stream, "ssm_scan_fwd_static launch");
 }
 
 }  // extern "C"

@@ -77,4 +77,40 @@ cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, 
     return cudaGetLastError();
 }
 
+// The conv history a later call needs: the last W1 = conv_width - 1 inputs of every row, reaching back
+// into the row's previous history when L < W1 (a chunked prefill or the first decode steps carry it
+// on; dpshk.com/news/5205047 section 1.3).  One thread per row; each thread reads all its sources
+// (plain loads: the history may be the output buffer) before it writes.
+template <typename T>
+__global__ void __launch_bounds__(kConvThreads) conv_history_kernel(const void* __restrict__ x, const void* conv_init,
+                                                                    void* conv_final, size_t rows, int L, int W1) {
+    using S = typename T::storage;
+    const size_t r = (size_t)blockIdx.x * kConvThreads + threadIdx.x;
+    if (r >= rows) return;
+    const S* xr = static_cast<const S*>(x) + r * (size_t)L;
+    const S* hi = conv_init != nullptr ? static_cast<const S*>(conv_init) + r * W1 : nullptr;
+    S v[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int t = L - W1 + i;
+        v[i] = S(0);
+        if (i < W1) v[i] = t >= 0 ? xr[t] : (hi != nullptr ? hi[W1 + t] : S(0));
+    }
+    S* out = static_cast<S*>(conv_final) + r * W1;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (i < W1) out[i] = v[i];
+}
+
+cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, size_t rows, int L, int W1,
+                                int dtype, cudaStream_t stream) {
+    if (W1 < 1 || W1 > 3) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)((rows + kConvThreads - 1) / kConvThreads);
+    if (dtype == 1)
+        conv_history_kernel<BF16><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, rows, L, W1);
+    else
+        conv_history_kernel<F32><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, rows, L, W1);
+    return cudaGetLastError();
+}
+
 }  // namespace ssm

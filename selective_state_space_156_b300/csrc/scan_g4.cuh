@@ -346,6 +346,16 @@ __global__ void __launch_bounds__(kG4Threads, 7) scan_g4_kernel(const ScanKernel
             }
         }
         if (c0 + kG4Chunk < t_end) g4_issue_chunk<NSL>(a, sm, buf ^ 1, b, ch0, c0 + kG4Chunk, has_z);
+        if (kConv && c0 == 0 && a.conv_init != nullptr) {
+            // x before t = 0 is the caller's history (oldest first), not the zeros the copy filled in
+            const int W1 = a.conv_width - 1;
+            for (int i = tid; i < kG4Chan * W1; i += kG4Threads) {
+                const int r = i / W1, k = i - r * W1;
+                if (ch0 + r < a.D)
+                    sm.x[buf][r][kG4Halo - W1 + k] =
+                        static_cast<const uint16_t*>(a.conv_init)[((size_t)b * a.D + ch0 + r) * W1 + k];
+            }
+        }
         // widen B / C of this chunk to fp32, in lane order
         for (int i = tid; i < 2 * kG4Chunk * 4; i += kG4Threads) {
             const int w = i / (kG4Chunk * 4);

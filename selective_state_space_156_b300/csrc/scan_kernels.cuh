@@ -210,14 +210,17 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
     cc.dskip = (a.Dskip != nullptr && active) ? __ldg(a.Dskip + d) : 0.0f;
     cc.bias = (a.delta_bias != nullptr && active) ? __ldg(a.delta_bias + d) : 0.0f;
 
-    // Conv history x_{t-3}, x_{t-2}, x_{t-1} at the segment start (zero before t = 0).
+    // Conv history x_{t-3}, x_{t-2}, x_{t-1} at the segment start: before t = 0 it is the caller's
+    // conv_init (the last W - 1 inputs of the previous call, oldest first), else zero.
     float xh[3] = {0.0f, 0.0f, 0.0f};
     if (a.conv_w != nullptr && active) {
         const size_t rowoff = row * (size_t)a.L;
+        const int W1 = a.conv_width - 1;
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
             const int t = t_begin - 3 + k;
             if (t >= 0) xh[k] = load1<Tin>(a.u, rowoff + t);
+            else if (a.conv_init != nullptr && t >= -W1) xh[k] = load1<Tin>(a.conv_init, row * W1 + W1 + t);
         }
     }
 

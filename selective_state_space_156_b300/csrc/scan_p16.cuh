@@ -336,6 +336,16 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();  // chunk c0 landed for every thread; everyone is done with the other buffers
         if (c0 + kP16Chunk < t_end) p16_issue_chunk<NS, LPC>(a, sm, buf ^ 1, b, ch0, c0 + kP16Chunk, has_z);
+        if (kConv && c0 == 0 && a.conv_init != nullptr) {
+            // x before t = 0 is the caller's history (oldest first), not the zeros the copy filled in
+            const int W1 = a.conv_width - 1;
+            for (int i = tid; i < kCh * W1; i += kP16Threads) {
+                const int r = i / W1, k = i - r * W1;
+                if (ch0 + r < a.D)
+                    sm.x[buf][r][kP16Halo - W1 + k] =
+                        static_cast<const uint16_t*>(a.conv_init)[((size_t)b * a.D + ch0 + r) * W1 + k];
+            }
+        }
         // widen B / C of this chunk to fp32 (consecutive threads write consecutive floats)
         for (int i = tid; i < 2 * NS * kP16Chunk; i += kP16Threads) {
             const int t = i / (2 * NS);

@@ -24,6 +24,7 @@ struct ScanKernelArgs {
     const float* conv_w;
     const float* conv_b;
     int conv_width;
+    const void* conv_init;  // (B*D, conv_width - 1) x before t = 0 (in dtype), or NULL for zeros
     const float* h0;
     float* h_out;
     void* y;
@@ -48,22 +49,39 @@ constexpr int kScanChunk = 64;     // timesteps of B/C staged in shared memory a
 // Launches the summary (when nseg > 1) and final scan kernels.  in/out: 0 = f32, 1 = bf16.
 cudaError_t launch_scan(const ScanKernelArgs& a, int in_dtype, int out_dtype, int zoh, cudaStream_t stream);
 
+// conv_final[r, i] = x_{L - W1 + i} of row r (from conv_init where that time is negative, zero without
+// it), W1 = conv_width - 1, for rows * W1 elements; conv_final may be conv_init itself.
+cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, size_t rows, int L, int W1,
+                                int dtype, cudaStream_t stream);
+
 cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, void* y, int Bsz, int D, int L,
                                  int width, int silu, int dtype, cudaStream_t stream);
 
-cudaError_t launch_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
-                                int Bsz, int D, int N, int softplus, int zoh, int dtype, cudaStream_t stream);
+// One decode step after host-side validation.  x is u, or the conv input when conv_w != NULL.
+struct DecodeStep {
+    float* state;
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* Bm;
+    const void* Cm;
+    const float* Dskip;
+    const float* delta_bias;
+    const void* z;
+    void* y;
+    const float* conv_w;  // (D, conv_width) or NULL
+    const float* conv_b;  // (D) or NULL
+    void* conv_state;     // (B, D, conv_width - 1) or NULL (conv_width == 1)
+    int conv_width;
+    int Bsz, D, N, softplus, zoh, dtype;  // dtype: 0 = f32, 1 = bf16
+};
+
+cudaError_t launch_state_update(const DecodeStep& s, cudaStream_t stream);
 
 // The streamed decode kernel (state_update_bulk.cu): eligibility, launch, and the flag its bounded
 // waits set on a timeout (read and cleared by take_bulk_wait_error, which synchronises).
-bool state_update_bulk_eligible(const float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, int D,
-                                int N);
-cudaError_t launch_state_update_bulk(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                     const void* Cm, const float* Dskip, const float* delta_bias, const void* z,
-                                     void* y, int Bsz, int D, int N, int softplus, int zoh, int dtype,
-                                     cudaStream_t stream);
+bool state_update_bulk_eligible(const DecodeStep& s);
+cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream);
 cudaError_t take_bulk_wait_error(unsigned* flags);
 
 // Launch geometry of each kernel kind, used by the host to plan the L split.

@@ -47,14 +47,10 @@ __device__ __forceinline__ void load4<BF16>(const void* base, size_t i, bool vec
 // are computed by both lanes; the readout is summed over the two lanes with one shuffle and lane 0
 // applies the D skip and the gate.  Zero-order hold as in the scan: h' = Abar (h - ng) + ng with
 // ng = -(v / a) B, exact at the fixed point; a == 0 uses the limit dt B.
-template <typename T, int NSL, bool kZOH>
-__global__ void __launch_bounds__(kDecThreads) state_update_kernel(float* __restrict__ state, const void* __restrict__ u,
-                                                                   const void* __restrict__ delta, const float* __restrict__ A,
-                                                                   const void* __restrict__ Bm, const void* __restrict__ Cm,
-                                                                   const float* __restrict__ Dskip,
-                                                                   const float* __restrict__ delta_bias,
-                                                                   const void* __restrict__ z, void* __restrict__ y, int D,
-                                                                   int N, int softplus_on, int vec) {
+template <typename T, int NSL, bool kZOH, bool kConv>
+__global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeStep s, int vec) {
+    float* __restrict__ state = s.state;
+    const int D = s.D, N = s.N;
     const int e = threadIdx.x & (kDecLanes - 1);
     const int d = blockIdx.x * (kDecThreads / kDecLanes) + threadIdx.x / kDecLanes;
     const bool active = d < D;
@@ -76,33 +72,60 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(float* __rest
         }
         float t4[4];
         if (full) {
-            load4<F32>(A, (size_t)d * N + n0, true, t4);
+            load4<F32>(s.A, (size_t)d * N + n0, true, t4);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) t4[i] = (active && n0 + i < N) ? __ldg(A + (size_t)d * N + n0 + i) : 0.0f;
+            for (int i = 0; i < 4; ++i) t4[i] = (active && n0 + i < N) ? __ldg(s.A + (size_t)d * N + n0 + i) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) av[4 * k + i] = t4[i];
         if (full) {
-            load4<T>(Bm, (size_t)b * N + n0, true, t4);
+            load4<T>(s.Bm, (size_t)b * N + n0, true, t4);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) t4[i] = (n0 + i < N) ? load1<T>(Bm, (size_t)b * N + n0 + i) : 0.0f;
+            for (int i = 0; i < 4; ++i) t4[i] = (n0 + i < N) ? load1<T>(s.Bm, (size_t)b * N + n0 + i) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) Bt[4 * k + i] = t4[i];
         if (full) {
-            load4<T>(Cm, (size_t)b * N + n0, true, t4);
+            load4<T>(s.Cm, (size_t)b * N + n0, true, t4);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) t4[i] = (n0 + i < N) ? load1<T>(Cm, (size_t)b * N + n0 + i) : 0.0f;
+            for (int i = 0; i < 4; ++i) t4[i] = (n0 + i < N) ? load1<T>(s.Cm, (size_t)b * N + n0 + i) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) Ct[4 * k + i] = t4[i];
     }
-    const float uv = active ? load1<T>(u, row) : 0.0f;
-    const float s = (active ? load1<T>(delta, row) : 0.0f) + ((delta_bias != nullptr && active) ? __ldg(delta_bias + d) : 0.0f);
-    const float dt = softplus_on ? softplus(s) : s;
+    float uv = active ? load1<T>(s.x, row) : 0.0f;
+    if (kConv) {
+        // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}) with x before t from the row's conv state (oldest
+        // first); both lanes of the row read the state before lane 0 writes the shifted one back
+        using Sx = typename T::storage;
+        const int W = s.conv_width, W1 = W - 1;
+        Sx* cs = static_cast<Sx*>(s.conv_state) + row * W1;
+        float c = (s.conv_b != nullptr && active) ? __ldg(s.conv_b + d) : 0.0f;
+        Sx hist[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            hist[k] = (active && k < W1) ? cs[k] : Sx(0);  // plain loads: this kernel writes the state back
+            float hv;
+            if constexpr (T::kBytes == 2) hv = bf16_to_f32(hist[k]);
+            else hv = hist[k];
+            if (active && k < W1) c = fmaf(__ldg(s.conv_w + (size_t)d * W + k), hv, c);
+        }
+        if (active) c = fmaf(__ldg(s.conv_w + (size_t)d * W + W1), uv, c);
+        __syncwarp();
+        if (active && e == 0) {
+            const Sx xraw = static_cast<const Sx*>(s.x)[row];
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+                if (k < W1) cs[k] = k + 1 < W1 ? hist[k + 1] : xraw;
+        }
+        uv = silu(c);
+    }
+    const float sr = (active ? load1<T>(s.delta, row) : 0.0f) +
+                     ((s.delta_bias != nullptr && active) ? __ldg(s.delta_bias + d) : 0.0f);
+    const float dt = s.softplus ? softplus(sr) : sr;
 
     float yp = 0.0f;
 #pragma unroll
@@ -125,9 +148,9 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(float* __rest
     for (int m = 1; m < kDecLanes; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
     if (!active) return;
     if (e == 0) {
-        const float gate = z != nullptr ? silu(load1<T>(z, row)) : 1.0f;
-        const float dsk = Dskip != nullptr ? __ldg(Dskip + d) : 0.0f;
-        store1<T>(y, row, fmaf(dsk, uv, yp) * gate);
+        const float gate = s.z != nullptr ? silu(load1<T>(s.z, row)) : 1.0f;
+        const float dsk = s.Dskip != nullptr ? __ldg(s.Dskip + d) : 0.0f;
+        store1<T>(s.y, row, fmaf(dsk, uv, yp) * gate);
     }
 #pragma unroll
     for (int k = 0; k < NSL / 4; ++k) {
@@ -144,36 +167,34 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(float* __rest
 }
 
 template <typename T, int NSL>
-static cudaError_t launch_su_ns(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
-                                int Bsz, int D, int N, int softplus_on, int zoh, cudaStream_t stream) {
+static cudaError_t launch_su_ns(const DecodeStep& s, cudaStream_t stream) {
     // vector loads need every lane's first state aligned: N % 4 == 0 and aligned bases (16 bytes for the
     // fp32 state and A, 4 elements for B and C)
     const int esz = sizeof(typename T::storage);
-    const int vec_state = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(state) & 15) == 0) &&
-                          ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
-                          ((reinterpret_cast<uintptr_t>(Bm) & (4 * esz - 1)) == 0) &&
-                          ((reinterpret_cast<uintptr_t>(Cm) & (4 * esz - 1)) == 0);
+    const int vec_state = (s.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(s.state) & 15) == 0) &&
+                          ((reinterpret_cast<uintptr_t>(s.A) & 15) == 0) &&
+                          ((reinterpret_cast<uintptr_t>(s.Bm) & (4 * esz - 1)) == 0) &&
+                          ((reinterpret_cast<uintptr_t>(s.Cm) & (4 * esz - 1)) == 0);
     dim3 block(kDecThreads);
-    dim3 grid((unsigned)((D + kDecThreads / kDecLanes - 1) / (kDecThreads / kDecLanes)), (unsigned)Bsz);
-    if (zoh)
-        state_update_kernel<T, NSL, true><<<grid, block, 0, stream>>>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, D,
-                                                                      N, softplus_on, vec_state);
-    else
-        state_update_kernel<T, NSL, false><<<grid, block, 0, stream>>>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y,
-                                                                       D, N, softplus_on, vec_state);
+    dim3 grid((unsigned)((s.D + kDecThreads / kDecLanes - 1) / (kDecThreads / kDecLanes)), (unsigned)s.Bsz);
+    const bool conv = s.conv_w != nullptr;
+    if (s.zoh) {
+        if (conv) state_update_kernel<T, NSL, true, true><<<grid, block, 0, stream>>>(s, vec_state);
+        else state_update_kernel<T, NSL, true, false><<<grid, block, 0, stream>>>(s, vec_state);
+    } else {
+        if (conv) state_update_kernel<T, NSL, false, true><<<grid, block, 0, stream>>>(s, vec_state);
+        else state_update_kernel<T, NSL, false, false><<<grid, block, 0, stream>>>(s, vec_state);
+    }
     return cudaGetLastError();
 }
 
 template <typename T>
-static cudaError_t launch_su_t(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                               const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
-                               int Bsz, int D, int N, int softplus_on, int zoh, cudaStream_t stream) {
+static cudaError_t launch_su_t(const DecodeStep& s, cudaStream_t stream) {
     // states per lane: N / kDecLanes rounded up to a multiple of 4
-    if (N <= 8) return launch_su_ns<T, 4>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
-    if (N <= 16) return launch_su_ns<T, 8>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
-    if (N <= 32) return launch_su_ns<T, 16>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
-    return launch_su_ns<T, 32>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
+    if (s.N <= 8) return launch_su_ns<T, 4>(s, stream);
+    if (s.N <= 16) return launch_su_ns<T, 8>(s, stream);
+    if (s.N <= 32) return launch_su_ns<T, 16>(s, stream);
+    return launch_su_ns<T, 32>(s, stream);
 }
 
 // SSM_DECODE_KERNEL=rows keeps every call on the row kernel above (for comparisons); by default calls
@@ -186,15 +207,10 @@ static bool bulk_decode_enabled() {
     return on;
 }
 
-cudaError_t launch_state_update(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, void* y,
-                                int Bsz, int D, int N, int softplus_on, int zoh, int dtype, cudaStream_t stream) {
-    if (bulk_decode_enabled() && state_update_bulk_eligible(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, D, N))
-        return launch_state_update_bulk(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh,
-                                        dtype, stream);
-    if (dtype == 1)
-        return launch_su_t<BF16>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
-    return launch_su_t<F32>(state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, N, softplus_on, zoh, stream);
+cudaError_t launch_state_update(const DecodeStep& s, cudaStream_t stream) {
+    if (bulk_decode_enabled() && state_update_bulk_eligible(s)) return launch_state_update_bulk(s, stream);
+    if (s.dtype == 1) return launch_su_t<BF16>(s, stream);
+    return launch_su_t<F32>(s, stream);
 }
 
 }  // namespace ssm

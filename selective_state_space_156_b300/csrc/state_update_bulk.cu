@@ -38,7 +38,7 @@ __device__ unsigned int g_bulk_wait_error = 0;
 
 constexpr int round16(int x) { return (x + 15) & ~15; }
 
-template <typename T, int N>
+template <typename T, int N, bool kConv>
 struct BulkLayout {
     static constexpr int kE = T::kBytes;
     static constexpr int kState = kTileRows * N * 4;
@@ -53,7 +53,11 @@ struct BulkLayout {
     static constexpr int kOffC = kOffB + kBC;
     static constexpr int kOffD = kOffC + kBC;
     static constexpr int kOffBias = kOffD + kTileRows * 4;
-    static constexpr int kBytes = round16(kOffBias + kTileRows * 4);
+    // conv front end (kConv): the rows' conv states (W - 1 <= 3 inputs each), taps (W <= 4) and biases
+    static constexpr int kOffCS = round16(kOffBias + kTileRows * 4);
+    static constexpr int kOffCW = kOffCS + (kConv ? round16(kTileRows * 3 * kE) : 0);
+    static constexpr int kOffCB = kOffCW + (kConv ? kTileRows * 4 * 4 : 0);
+    static constexpr int kBytes = round16(kOffCB + (kConv ? kTileRows * 4 : 0));
     static constexpr int kStages = N <= 32 ? 4 : 3;
     static constexpr int kSmem = 128 + kStages * kBytes;  // barriers and counters first
 };
@@ -69,6 +73,10 @@ struct DecodeArgs {
     const float* delta_bias;
     const void* z;
     void* y;
+    const float* conv_w;  // (D, W) or NULL
+    const float* conv_b;  // (D) or NULL
+    void* conv_state;     // (B, D, W - 1), read and written; NULL when W == 1
+    int W;
     int Bsz, D, softplus;
 };
 
@@ -92,9 +100,9 @@ __device__ __forceinline__ void smem_vec4(const unsigned char* base, int i, floa
     }
 }
 
-template <typename T, int N, bool kZOH>
+template <typename T, int N, bool kZOH, bool kConv>
 __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(const DecodeArgs a) {
-    using L = BulkLayout<T, N>;
+    using L = BulkLayout<T, N, kConv>;
     constexpr int S = L::kStages;
     constexpr int E = L::kE;
     constexpr int TPR = N / 4;                  // threads per row
@@ -141,9 +149,18 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
                 uint64_t* bar = &full[s];
                 unsigned char* st = stages + s * L::kBytes;
                 const unsigned sb = (unsigned)(rows * N * 4), eb = (unsigned)(rows * E), pb = (unsigned)(rows * 4);
-                const unsigned bytes = 2 * sb + 2 * eb + (a.z ? eb : 0u) + 2u * N * E + (a.Dskip ? pb : 0u) +
-                                       (a.delta_bias ? pb : 0u);
+                unsigned bytes = 2 * sb + 2 * eb + (a.z ? eb : 0u) + 2u * N * E + (a.Dskip ? pb : 0u) +
+                                 (a.delta_bias ? pb : 0u);
+                const unsigned csb = (unsigned)(rows * (a.W - 1) * E), cwb = (unsigned)(rows * a.W * 4);
+                if (kConv) bytes += (a.W > 1 ? csb : 0u) + cwb + (a.conv_b ? pb : 0u);
                 mbar_arrive_expect_tx(bar, bytes);
+                if (kConv) {
+                    if (a.W > 1)
+                        bulk_g2s(st + L::kOffCS, static_cast<const unsigned char*>(a.conv_state) + r0 * (a.W - 1) * E,
+                                 csb, bar);
+                    bulk_g2s(st + L::kOffCW, a.conv_w + (size_t)d0 * a.W, cwb, bar);
+                    if (a.conv_b) bulk_g2s(st + L::kOffCB, a.conv_b + d0, pb, bar);
+                }
                 bulk_g2s(st + L::kOffState, a.state + r0 * N, sb, bar);
                 bulk_g2s(st + L::kOffA, a.A + (size_t)d0 * N, sb, bar);
                 bulk_g2s(st + L::kOffU, static_cast<const unsigned char*>(a.u) + r0 * E, eb, bar);
@@ -185,7 +202,28 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
                 const int r = p * RPP + tid / TPR;
                 const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + 4 * q);
                 const float4 av = *reinterpret_cast<const float4*>(As + r * N + 4 * q);
-                const float uv = smem_scalar<T>(st + L::kOffU, r);
+                float uv = smem_scalar<T>(st + L::kOffU, r);
+                if constexpr (kConv) {
+                    // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}); x before t is the row's conv state
+                    const int W1 = a.W - 1;
+                    const float* cw = reinterpret_cast<const float*>(st + L::kOffCW) + r * a.W;
+                    float c = a.conv_b ? reinterpret_cast<const float*>(st + L::kOffCB)[r] : 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        if (k < W1) c = fmaf(cw[k], smem_scalar<T>(st + L::kOffCS, r * W1 + k), c);
+                    c = fmaf(cw[W1], uv, c);
+                    if (q == 0 && r < rows) {
+                        // the new conv state: the last W - 1 inputs, oldest first (raw values, no rounding)
+                        using Sx = typename T::storage;
+                        const Sx* cs = reinterpret_cast<const Sx*>(st + L::kOffCS) + r * W1;
+                        Sx* out = static_cast<Sx*>(a.conv_state) + (r0 + r) * W1;
+#pragma unroll
+                        for (int k = 0; k < 3; ++k)
+                            if (k < W1) out[k] = k + 1 < W1 ? cs[k + 1] : reinterpret_cast<const Sx*>(st + L::kOffU)[r];
+                    }
+                    if constexpr (T::kBytes == 2) uv = silu_fast(c);
+                    else uv = silu(c);
+                }
                 const float sr = smem_scalar<T>(st + L::kOffDt, r) + (a.delta_bias ? bs[r] : 0.0f);
                 const float zr = a.z ? smem_scalar<T>(st + L::kOffZ, r) : 0.0f;
                 const float dsk = a.Dskip ? Ds[r] : 0.0f;
@@ -237,10 +275,10 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
     }
 }
 
-template <typename T, int N, bool kZOH>
+template <typename T, int N, bool kZOH, bool kConv>
 cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
-    using L = BulkLayout<T, N>;
-    auto kfn = state_update_bulk_kernel<T, N, kZOH>;
+    using L = BulkLayout<T, N, kConv>;
+    auto kfn = state_update_bulk_kernel<T, N, kZOH, kConv>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -255,7 +293,8 @@ cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
 
 template <typename T, int N>
 cudaError_t launch_bulk_n(const DecodeArgs& a, int zoh, cudaStream_t s) {
-    return zoh ? launch_bulk<T, N, true>(a, s) : launch_bulk<T, N, false>(a, s);
+    if (a.conv_w != nullptr) return zoh ? launch_bulk<T, N, true, true>(a, s) : launch_bulk<T, N, false, true>(a, s);
+    return zoh ? launch_bulk<T, N, true, false>(a, s) : launch_bulk<T, N, false, false>(a, s);
 }
 
 template <typename T>
@@ -272,22 +311,21 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
 
-bool state_update_bulk_eligible(const float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                const void* Cm, const float* Dskip, const float* delta_bias, const void* z, int D,
-                                int N) {
-    if (N != 8 && N != 16 && N != 32 && N != 64) return false;
-    if (D % 8 != 0) return false;
-    return al16(state) && al16(u) && al16(delta) && al16(A) && al16(Bm) && al16(Cm) && (!Dskip || al16(Dskip)) &&
-           (!delta_bias || al16(delta_bias)) && (!z || al16(z));
+bool state_update_bulk_eligible(const DecodeStep& s) {
+    if (s.N != 8 && s.N != 16 && s.N != 32 && s.N != 64) return false;
+    if (s.D % 8 != 0) return false;
+    const bool conv_ok = !s.conv_w || (al16(s.conv_w) && (!s.conv_b || al16(s.conv_b)) &&
+                                       (s.conv_width == 1 || al16(s.conv_state)));
+    return al16(s.state) && al16(s.x) && al16(s.delta) && al16(s.A) && al16(s.Bm) && al16(s.Cm) &&
+           (!s.Dskip || al16(s.Dskip)) && (!s.delta_bias || al16(s.delta_bias)) && (!s.z || al16(s.z)) && conv_ok;
 }
 
-cudaError_t launch_state_update_bulk(float* state, const void* u, const void* delta, const float* A, const void* Bm,
-                                     const void* Cm, const float* Dskip, const float* delta_bias, const void* z,
-                                     void* y, int Bsz, int D, int N, int softplus_on, int zoh, int dtype,
-                                     cudaStream_t stream) {
-    const DecodeArgs a{state, u, delta, A, Bm, Cm, Dskip, delta_bias, z, y, Bsz, D, softplus_on};
-    if (dtype == 1) return launch_bulk_t<BF16>(a, N, zoh, stream);
-    return launch_bulk_t<F32>(a, N, zoh, stream);
+cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream) {
+    const DecodeArgs a{s.state, s.x, s.delta, s.A, s.Bm, s.Cm, s.Dskip, s.delta_bias, s.z, s.y,
+                       s.conv_w, s.conv_w ? s.conv_b : nullptr, s.conv_w ? s.conv_state : nullptr,
+                       s.conv_w ? s.conv_width : 1, s.Bsz, s.D, s.softplus};
+    if (s.dtype == 1) return launch_bulk_t<BF16>(a, s.N, s.zoh, stream);
+    return launch_bulk_t<F32>(a, s.N, s.zoh, stream);
 }
 
 cudaError_t take_bulk_wait_error(unsigned* flags) {

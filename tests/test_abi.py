@@ -50,30 +50,46 @@ def test_version_string(L):
     assert b"sm_103a" in L.ssm_version()
 
 
-def test_params_struct_layout_matches_c():
+def _c_layout(struct: str, fields: str) -> dict:
     src = r"""
 #include <stdio.h>
 #include <stddef.h>
 #include "ssm_scan.h"
-#define F(f) printf(#f " %zu\n", offsetof(ssm_scan_params, f));
+#define F(f) printf(#f " %zu\n", offsetof(STRUCT, f));
 int main(void) {
-  printf("sizeof %zu\n", sizeof(ssm_scan_params));
-  F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(out_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip)
-  F(delta_bias) F(z) F(conv_w) F(conv_b) F(conv_width) F(h0) F(h_out) F(y) F(delta_softplus) F(zoh)
-  F(workspace) F(workspace_bytes)
+  printf("sizeof %zu\n", sizeof(STRUCT));
+  FIELDS
   return 0;
 }
-"""
+""".replace("STRUCT", struct).replace("FIELDS", fields)
     with tempfile.TemporaryDirectory() as td:
         c = os.path.join(td, "layout.c")
         exe = os.path.join(td, "layout")
         open(c, "w").write(src)
         subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", exe, c], check=True)
         out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
-    got = dict(l.split() for l in out.splitlines())
+    return dict(l.split() for l in out.splitlines())
+
+
+def test_params_struct_layout_matches_c():
+    got = _c_layout("ssm_scan_params", """
+  F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(out_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip)
+  F(delta_bias) F(z) F(conv_w) F(conv_b) F(conv_width) F(h0) F(h_out) F(y) F(delta_softplus) F(zoh)
+  F(workspace) F(workspace_bytes) F(conv_init) F(conv_final)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanParams)
+    assert len(got) == len(ssm.ScanParams._fields_)
     for name, off in got.items():
         assert getattr(ssm.ScanParams, name).offset == int(off), name
+
+
+def test_step_params_struct_layout_matches_c():
+    got = _c_layout("ssm_step_params", """
+  F(batch) F(dim) F(dstate) F(dtype) F(state) F(x) F(delta) F(A) F(Bm) F(Cm) F(Dskip) F(delta_bias) F(z)
+  F(conv_w) F(conv_b) F(conv_width) F(conv_state) F(y) F(delta_softplus) F(zoh)""")
+    assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.StepParams)
+    assert len(got) == len(ssm.StepParams._fields_)
+    for name, off in got.items():
+        assert getattr(ssm.StepParams, name).offset == int(off), name
 
 
 def _params(**kw):
@@ -141,3 +157,45 @@ def test_calls_without_library_fail_loudly(monkeypatch):
     monkeypatch.setattr(ssm, "LIB_PATH", "/nonexistent/libssm_b300.so")
     with pytest.raises(ImportError):
         ssm.lib()
+
+
+def _step(**kw):
+    p = ssm.StepParams()
+    p.batch, p.dim, p.dstate, p.dtype = 4, 64, 16, ssm.SSM_BF16
+    fake = 1 << 40  # never dereferenced: every case below fails validation before any launch
+    p.state, p.x, p.delta, p.A, p.Bm, p.Cm = (fake + (i << 30) for i in range(6))
+    p.y = fake + (6 << 30)
+    p.conv_w = fake + (7 << 30)
+    p.conv_width = 4
+    p.conv_state = fake + (8 << 30)
+    p.delta_softplus, p.zoh = 1, 1
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("conv_width", 5, ssm.SSM_ERR_INVALID_ARG),
+    ("conv_width", 0, ssm.SSM_ERR_INVALID_ARG),
+    ("conv_state", None, ssm.SSM_ERR_INVALID_ARG),
+    ("dstate", 48, ssm.SSM_ERR_UNSUPPORTED),
+    ("x", None, ssm.SSM_ERR_INVALID_ARG),
+    ("dtype", 3, ssm.SSM_ERR_INVALID_ARG),
+])
+def test_conv_step_rejects_bad_arguments_on_host(L, field, value, status):
+    p = _step(**{field: value})
+    assert L.ssm_state_update_conv(ctypes.byref(p), None) == status
+    assert L.ssm_last_error().decode().startswith("ssm_state_update_conv")
+
+
+def test_conv_step_rejects_overlapping_conv_state(L):
+    p = _step()
+    p.conv_state = p.x + 8  # starts inside x
+    assert L.ssm_state_update_conv(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "conv_state overlaps" in L.ssm_last_error().decode()
+
+
+def test_scan_rejects_conv_final_overlapping_an_input(L):
+    p = _params(conv_w=(1 << 40) + (7 << 30), conv_width=4, conv_final=(1 << 40) + 64)  # inside u
+    assert L.ssm_scan_fwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "conv_final overlaps" in L.ssm_last_error().decode()
