@@ -9,10 +9,11 @@
 // their u, delta, z, D skip and dt bias, and the batch row's B and C.  One producer warp issues the
 // copies of each tile once the four consumer warps have released its stage (an "empty" mbarrier per
 // stage, one arrival per warp); consumers wait on the stage's "full" mbarrier (the copies' byte
-// count), so no warp waits on another except through the ring.  Consumer thread t of the 128 owns the
-// four states 4 (t mod N/4) .. +3 of a row; a warp therefore reads and writes whole 512-byte runs of
-// the state.  The new state leaves with 16-byte streaming stores straight from registers; y leaves
-// from the first lane of each row.
+// count), so no warp waits on another except through the ring.  A row belongs to 2 consumer threads
+// (N / 8 for N > 16), each with 8 consecutive states (4 for N = 8): the per-row scalars (softplus,
+// gate, conv) are computed by few threads, and a warp still reads and writes whole rows of the state.
+// The new state leaves with 16-byte streaming stores straight from registers; y leaves from the first
+// thread of each row.
 //
 // Requirements (the host checks them before choosing this kernel): N in {8, 16, 32, 64}, D % 8 == 0
 // (every tile's row count is a multiple of 8, so every copy is a multiple of 16 bytes) and 16-byte
@@ -101,11 +102,12 @@ __device__ __forceinline__ void smem_vec4(const unsigned char* base, int i, floa
 }
 
 template <typename T, int N, bool kZOH, bool kConv>
-__global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel(const DecodeArgs a) {
     using L = BulkLayout<T, N, kConv>;
     constexpr int S = L::kStages;
     constexpr int E = L::kE;
-    constexpr int TPR = N / 4;                  // threads per row
+    constexpr int TPR = N <= 16 ? 2 : N / 8;   // threads per row
+    constexpr int SL = N / TPR;                 // states per thread: 4 (N = 8) or 8
     constexpr int RPP = kBulkThreads / TPR;     // rows per pass
     constexpr int kWarps = kBulkThreads / 32;   // consumer warps
     extern __shared__ __align__(128) unsigned char bulk_smem[];
@@ -192,16 +194,31 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
             const float* As = reinterpret_cast<const float*>(st + L::kOffA);
             const float* Ds = reinterpret_cast<const float*>(st + L::kOffD);
             const float* bs = reinterpret_cast<const float*>(st + L::kOffBias);
-            float Bv[4], Cv[4];
-            smem_vec4<T>(st + L::kOffB, 4 * q, Bv);
-            smem_vec4<T>(st + L::kOffC, 4 * q, Cv);
+            // this thread's states are SL * q .. SL * q + SL - 1 (whole 16-byte chunks of a row)
+            float Bv[SL], Cv[SL];
+#pragma unroll
+            for (int c = 0; c < SL / 4; ++c) {
+                float t4[4];
+                smem_vec4<T>(st + L::kOffB, SL * q + 4 * c, t4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Bv[4 * c + i] = t4[i];
+                smem_vec4<T>(st + L::kOffC, SL * q + 4 * c, t4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Cv[4 * c + i] = t4[i];
+            }
 #pragma unroll
             for (int p = 0; p < kTileRows / RPP; ++p) {
                 // every lane takes part in the shuffles; rows past the tile's end compute on stale values
                 // and store nothing
                 const int r = p * RPP + tid / TPR;
-                const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + 4 * q);
-                const float4 av = *reinterpret_cast<const float4*>(As + r * N + 4 * q);
+                float h[SL], A4[SL];
+#pragma unroll
+                for (int c = 0; c < SL / 4; ++c) {
+                    const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + SL * q + 4 * c);
+                    const float4 av = *reinterpret_cast<const float4*>(As + r * N + SL * q + 4 * c);
+                    h[4 * c] = hv.x; h[4 * c + 1] = hv.y; h[4 * c + 2] = hv.z; h[4 * c + 3] = hv.w;
+                    A4[4 * c] = av.x; A4[4 * c + 1] = av.y; A4[4 * c + 2] = av.z; A4[4 * c + 3] = av.w;
+                }
                 float uv = smem_scalar<T>(st + L::kOffU, r);
                 if constexpr (kConv) {
                     // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}); x before t is the row's conv state
@@ -235,12 +252,10 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
                     dt = a.softplus ? softplus(sr) : sr;
                     gate = a.z ? silu(zr) : 1.0f;
                 }
-                float h[4] = {hv.x, hv.y, hv.z, hv.w};
-                const float A4[4] = {av.x, av.y, av.z, av.w};
                 const float dtu = dt * uv;
                 float yp = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < SL; ++i) {
                     const float ab = ex2(dt * (A4[i] * kLog2e));
                     if (kZOH) {
                         // branch-free: the a -> 0 limit (Abar = 1, Bbar = dt B) is selected, not branched to
@@ -256,7 +271,10 @@ __global__ void __launch_bounds__(kBulkThreads + 32) state_update_bulk_kernel(co
 #pragma unroll
                 for (int m = 1; m < TPR; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
                 if (r < rows) {
-                    __stcs(reinterpret_cast<float4*>(a.state + (r0 + r) * N + 4 * q), make_float4(h[0], h[1], h[2], h[3]));
+#pragma unroll
+                    for (int c = 0; c < SL / 4; ++c)
+                        __stcs(reinterpret_cast<float4*>(a.state + (r0 + r) * N + SL * q + 4 * c),
+                               make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]));
                     if (q == 0) store1<T>(a.y, r0 + r, fmaf(dsk, uv, yp) * gate);
                 }
             }
