@@ -43,7 +43,7 @@ def _load():
         lib.oracle_scan_rows.restype = ctypes.c_int
         lib.oracle_scan_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, _ip,
                                          _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, _dp, _dp,
-                                         _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+                                         _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_conv1d_rows.restype = ctypes.c_int
         lib.oracle_conv1d_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, _dp, _dp, _dp,
                                            ctypes.c_int, _dp]
@@ -83,7 +83,8 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
     ``rows``: optional list of (b, d) pairs to compute; default is every row in (b, d) order.
     ``inputs["conv_init"]`` (B, D, W-1), when present with a conv, is the x history before t = 0.
     Returns (y (R, L), h_out (R, N), threads_used) as fp64 numpy arrays; with a dict ``extra`` and a
-    conv, also stores the last W-1 inputs of every row as ``extra["conv_final"]`` (R, W-1).
+    conv, also stores the last W-1 inputs of every row as ``extra["conv_final"]`` (R, W-1); with
+    ``extra["h_all"] = True`` it also stores the state after every step as ``extra["h_all"]`` (R, L, N).
     """
     lib = _load()
     Bsz, D, L = tuple(inputs["u"].shape)
@@ -127,15 +128,18 @@ def scan(inputs: dict, rows: Optional[Sequence[tuple]] = None, nthreads: int = 0
     cf = np.zeros((R, max(W - 1, 1)), dtype=np.float64) if (cw is not None and extra is not None) else None
     y = np.empty((R, L), dtype=np.float64)
     h_out = np.empty((R, N), dtype=np.float64)
+    h_all = np.empty((R, L, N), dtype=np.float64) if (extra is not None and extra.get("h_all")) else None
     z_flag = inputs.get("zoh", True) if zoh is None else zoh
     sp_flag = inputs.get("delta_softplus", True) if delta_softplus is None else delta_softplus
     nt = lib.oracle_scan_rows(R, L, N, _iptr(rb), _iptr(rd), _ptr(ur), _ptr(dr), _ptr(zr), _ptr(A), _ptr(Dskip),
                               _ptr(bias), _ptr(cw), _ptr(cb), W, _ptr(ci), _ptr(cf), _ptr(Bm), _ptr(Cm), _ptr(h0),
-                              _ptr(y), _ptr(h_out), int(bool(sp_flag)), int(bool(z_flag)), int(nthreads))
+                              _ptr(y), _ptr(h_out), _ptr(h_all), int(bool(sp_flag)), int(bool(z_flag)), int(nthreads))
     if nt < 0:
         raise ValueError("oracle_scan_rows rejected its arguments")
     if cf is not None:
         extra["conv_final"] = cf[:, :W - 1]
+    if h_all is not None:
+        extra["h_all"] = h_all
     return y, h_out, nt
 
 

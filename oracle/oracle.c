@@ -52,6 +52,7 @@ typedef struct {
     const double *conv_init;              /* (R, W-1): x before t = 0, or NULL     */
     double *conv_final;                   /* (R, W-1): the last W-1 x, or NULL     */
     double *y, *h_out;                    /* (R, L), (R, N) or NULL                */
+    double *h_all;                        /* (R, L, N): the state after every step, or NULL */
     int delta_softplus, zoh;
     int next_row;                         /* work counter, guarded by lock         */
     pthread_mutex_t lock;
@@ -110,6 +111,7 @@ static void scan_one_row(const scan_job *j, int r, double *h, double *v) {
                 Bbar = dt * Bt;
             h[n] = Abar * h[n] + Bbar * v[t];
             y += Cb[(size_t)n * L + t] * h[n];
+            if (j->h_all) j->h_all[((size_t)r * L + t) * N + n] = h[n];
         }
         if (j->Dskip) y += j->Dskip[d] * v[t];
         if (j->z) y *= silu(j->z[(size_t)r * L + t]);
@@ -147,7 +149,9 @@ static int resolve_threads(int nthreads, int R) {
 /*
  * Selective scan over R independent rows.  Row r is (batch row_b[r], channel row_d[r]);
  * its u/delta/z/y are the r-th length-L rows of the compact (R, L) arrays, and its
- * initial/final state the r-th N-vector of h0/h_out.  Passing all (b, d) pairs in order
+ * initial/final state the r-th N-vector of h0/h_out.  h_all (R, L, N), when given, receives
+ * the state after every step: the state sequence a multi-token verification pass keeps
+ * (pwwt.cn/news/5168881 section 3.4).  Passing all (b, d) pairs in order
  * makes the compact layout equal to the full (B, D, L) layout.
  * Returns the number of threads used, or -1 on bad arguments.
  */
@@ -157,7 +161,8 @@ ORACLE_API int oracle_scan_rows(int R, int L, int N, const int *row_b, const int
                                 const double *conv_w, const double *conv_b, int conv_width,
                                 const double *conv_init, double *conv_final,
                                 const double *Bm, const double *Cm, const double *h0,
-                                double *y, double *h_out, int delta_softplus, int zoh, int nthreads) {
+                                double *y, double *h_out, double *h_all, int delta_softplus, int zoh,
+                                int nthreads) {
     if (R < 0 || L < 0 || N <= 0 || !row_b || !row_d || !u || !delta || !A || !Bm || !Cm || !y) return -1;
     if (conv_w && (conv_width <= 0 || conv_width > 8)) return -1;
     scan_job j;
@@ -166,6 +171,7 @@ ORACLE_API int oracle_scan_rows(int R, int L, int N, const int *row_b, const int
     j.row_b = row_b; j.row_d = row_d;
     j.u = u; j.delta = delta; j.z = z; j.A = A; j.Dskip = Dskip; j.delta_bias = delta_bias;
     j.conv_w = conv_w; j.conv_b = conv_b; j.Bm = Bm; j.Cm = Cm; j.h0 = h0; j.y = y; j.h_out = h_out;
+    j.h_all = h_all;
     j.conv_init = conv_w ? conv_init : NULL;
     j.conv_final = conv_w ? conv_final : NULL;
     j.delta_softplus = delta_softplus; j.zoh = zoh;
@@ -225,7 +231,7 @@ ORACLE_API int oracle_state_update(int Bsz, int D, int N, double *state, const d
        state (B, D, N) is the compact (R, N) layout; scan_one_row copies h0 before it writes h_out,
        so passing the same buffer for both is safe. */
     int rc = oracle_scan_rows(R, 1, N, rb, rd, u, delta, z, A, Dskip, delta_bias, conv_w, conv_b, conv_width,
-                              conv_state, conv_state, Bm, Cm, state, y, state, delta_softplus, zoh, nthreads);
+                              conv_state, conv_state, Bm, Cm, state, y, state, NULL, delta_softplus, zoh, nthreads);
     free(rb);
     free(rd);
     return rc;

@@ -400,6 +400,35 @@ def test_p13_decode_with_conv_state_equals_fused_scan(W):
 
 
 # ---------------------------------------------------------------------------------------------
+# P14: the state sequence of a multi-token verification pass (pwwt.cn/news/5168881 3.4): the state
+# after step t equals the final state of the same scan cut after t + 1 steps
+# ---------------------------------------------------------------------------------------------
+def test_p14_state_sequence_equals_truncated_runs():
+    L = 9
+    d = _inputs(2, 3, 4, L, with_z=True, h0=True, seed=14)
+    extra = {"h_all": True}
+    y, h, _ = oracle.scan(d, extra=extra)
+    for t in range(L):
+        cut = dict(d, u=d["u"][..., :t + 1], delta=d["delta"][..., :t + 1], z=d["z"][..., :t + 1],
+                   Bm=d["Bm"][..., :t + 1], Cm=d["Cm"][..., :t + 1])
+        _, ht, _ = oracle.scan(cut)
+        np.testing.assert_array_equal(extra["h_all"][:, t, :], ht)
+    np.testing.assert_array_equal(extra["h_all"][:, -1, :], h)
+    # and the closed form of the state sequence, h_t = prod_{j<=t} Abar_j h0 + sum_{i<=t} prod_{i<j<=t} Abar_j
+    # Bbar_i u_i, from the definitions (no recurrence)
+    Abar, Bbar, _ = _disc(d)
+    u = _np(d, "u")
+    h0 = _np(d, "h0")
+    ref = np.zeros((2, 3, L, 4))
+    for t in range(L):
+        acc = np.prod(Abar[..., :t + 1], axis=-1) * h0
+        for i in range(t + 1):
+            acc = acc + np.prod(Abar[..., i + 1:t + 1], axis=-1) * Bbar[..., i] * u[:, :, None, i]
+        ref[:, :, t, :] = acc
+    np.testing.assert_allclose(extra["h_all"].reshape(2, 3, L, 4), ref, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------------
 # P10: N = 1, no D, simplified Bbar: scalar closed form y_k = c_k sum_i (prod_{j=i+1..k} a_j) b_i x_i
 # ---------------------------------------------------------------------------------------------
 def test_p10_scalar_closed_form():
