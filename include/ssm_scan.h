@@ -100,6 +100,18 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  *                   the next call's conv_init or the decode conv state; NULL if not wanted.  May be
  *                   the same buffer as conv_init; must not overlap any other tensor.  Ignored
  *                   without conv_w.
+ *   state_indices (B) int32, or NULL.  Per-request state slots (pwwt.cn/news/5168881 section 3.4:
+ *                   a state cache indexed by request): h0, h_out, conv_init and conv_final are then
+ *                   caches with a leading slot dimension, (S, D, N) and (S, D, W-1), and batch row b
+ *                   reads and writes slot state_indices[b].  A negative index marks a padding row:
+ *                   nothing of any slot is read or written for it and its y is written as zeros.  The
+ *                   caller guarantees indices < S and no index used twice.  Takes the element-wise
+ *                   kernel: dstate <= 16, no L split.
+ *   h_all       (B, L, D, N) float32, or NULL: receives the state after every step, the state
+ *                   sequence a multi-token verification pass keeps so that the caller can commit the
+ *                   state at the accepted length (pwwt.cn/news/5168881 section 3.4: speculative
+ *                   decoding).  Takes the element-wise kernel (dstate <= 16); must not overlap any
+ *                   other tensor; padding rows leave theirs untouched.
  */
 typedef struct ssm_scan_params {
     int batch, dim, dstate, seqlen;
@@ -124,6 +136,8 @@ typedef struct ssm_scan_params {
     size_t workspace_bytes;
     const void *conv_init;
     void *conv_final;
+    const int *state_indices;
+    float *h_all;
 } ssm_scan_params;
 
 /* Selective scan forward (with the optional fused conv front end, D skip and gate).
@@ -205,6 +219,10 @@ SSM_API ssm_status ssm_device_error(unsigned *flags);
  *   conv_width  int                  1..4 when conv_w != NULL
  *   conv_state  (B, D, conv_width-1) dtype, read and written in place; required when
  *                                    conv_width > 1; must not overlap any other tensor
+ *   state_indices (B) int32 or NULL: state and conv_state are then slot caches (S, D, N) and
+ *                                    (S, D, W-1) and batch row b uses slot state_indices[b]; a
+ *                                    negative index marks a padding row (no slot touched, y = 0).
+ *                                    Indices < S, none used twice (pwwt.cn/news/5168881 section 3.4)
  * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED (dstate), SSM_ERR_CUDA.
  */
 typedef struct ssm_step_params {
@@ -226,6 +244,7 @@ typedef struct ssm_step_params {
     void *y;
     int delta_softplus;
     int zoh;
+    const int *state_indices;
 } ssm_step_params;
 
 SSM_API ssm_status ssm_state_update_conv(const ssm_step_params *p, ssm_stream_t stream);

@@ -46,6 +46,7 @@ class ScanParams(ctypes.Structure):
         ("h_out", ctypes.c_void_p), ("y", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
         ("zoh", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("conv_init", ctypes.c_void_p), ("conv_final", ctypes.c_void_p),
+        ("state_indices", ctypes.c_void_p), ("h_all", ctypes.c_void_p),
     ]
 
 
@@ -58,6 +59,7 @@ class StepParams(ctypes.Structure):
         ("delta_bias", ctypes.c_void_p), ("z", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
         ("conv_b", ctypes.c_void_p), ("conv_width", ctypes.c_int), ("conv_state", ctypes.c_void_p),
         ("y", ctypes.c_void_p), ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int),
+        ("state_indices", ctypes.c_void_p),
     ]
 
 
@@ -125,8 +127,19 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _slots_shape(t, name, Bsz, tail, state_indices):
+    """Shape check of a tensor that is per batch row, or a slot cache (S, *tail) with state_indices."""
+    if t is None:
+        return None
+    if state_indices is None:
+        return (Bsz,) + tuple(tail)
+    if t.dim() != 1 + len(tail) or tuple(t.shape[1:]) != tuple(tail):
+        raise ValueError(f"{name} must be a slot cache (slots, {', '.join(map(str, tail))})")
+    return tuple(t.shape)
+
+
 def _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
-                 workspace, conv_init=None, conv_final=None) -> ScanParams:
+                 workspace, conv_init=None, conv_final=None, state_indices=None, h_all=None) -> ScanParams:
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
     Bsz, D, L = u.shape
@@ -153,10 +166,15 @@ def _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, 
         p.conv_width = conv_w.shape[1]
         p.conv_b = _ptr(conv_b, "conv_b", torch.float32, (D,))
         W1 = conv_w.shape[1] - 1
-        p.conv_init = _ptr(conv_init, "conv_init", idt, (Bsz, D, W1)) if W1 > 0 else None
-        p.conv_final = _ptr(conv_final, "conv_final", idt, (Bsz, D, W1)) if W1 > 0 else None
-    p.h0 = _ptr(h0, "h0", torch.float32, (Bsz, D, N))
-    p.h_out = _ptr(h_out, "h_out", torch.float32, (Bsz, D, N))
+        if W1 > 0:
+            p.conv_init = _ptr(conv_init, "conv_init", idt, _slots_shape(conv_init, "conv_init", Bsz, (D, W1),
+                                                                          state_indices))
+            p.conv_final = _ptr(conv_final, "conv_final", idt, _slots_shape(conv_final, "conv_final", Bsz, (D, W1),
+                                                                             state_indices))
+    p.h0 = _ptr(h0, "h0", torch.float32, _slots_shape(h0, "h0", Bsz, (D, N), state_indices))
+    p.h_out = _ptr(h_out, "h_out", torch.float32, _slots_shape(h_out, "h_out", Bsz, (D, N), state_indices))
+    p.state_indices = _ptr(state_indices, "state_indices", torch.int32, (Bsz,))
+    p.h_all = _ptr(h_all, "h_all", torch.float32, (Bsz, L, D, N))
     p.y = _ptr(y, "y", None, (Bsz, D, L)) if y is not None else None
     p.delta_softplus = int(bool(delta_softplus))
     p.zoh = int(bool(zoh))
@@ -173,7 +191,8 @@ def ssm_scan_workspace_size(u, delta, A, Bm, Cm, **kw) -> int:
         y = torch.empty_like(u, dtype=kw.pop("out_dtype", None) or u.dtype)
     p = _scan_params(u, delta, A, Bm, Cm, kw.get("Dskip"), kw.get("delta_bias"), kw.get("z"), kw.get("conv_w"),
                      kw.get("conv_b"), kw.get("h0"), kw.get("h_out"), y, kw.get("delta_softplus", True),
-                     kw.get("zoh", True), None, kw.get("conv_init"), kw.get("conv_final"))
+                     kw.get("zoh", True), None, kw.get("conv_init"), kw.get("conv_final"), kw.get("state_indices"),
+                     kw.get("h_all"))
     return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
 
 
@@ -184,24 +203,30 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
                  h_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
                  delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
                  workspace: Optional[torch.Tensor] = None, return_state: bool = False, stream=None,
-                 conv_init: Optional[torch.Tensor] = None, conv_final: Optional[torch.Tensor] = None):
+                 conv_init: Optional[torch.Tensor] = None, conv_final: Optional[torch.Tensor] = None,
+                 state_indices: Optional[torch.Tensor] = None, h_all: Optional[torch.Tensor] = None):
     """Selective scan forward on the GPU.  Layouts as in include/ssm_scan.h: u/delta/z/y (B, D, L),
     Bm/Cm (B, N, L), A (D, N) fp32, Dskip/delta_bias/conv_b (D,) fp32, conv_w (D, W) fp32,
     h0/h_out (B, D, N) fp32, conv_init/conv_final (B, D, W-1) of u's dtype (the conv history before
-    and after this call; conv_final may be conv_init).  ``workspace`` (uint8 CUDA tensor, optional)
-    enables the L split; pass ``workspace="auto"`` to allocate it here.  Returns y, or (y, h_out) with
-    return_state."""
+    and after this call; conv_final may be conv_init).  ``state_indices`` (B,) int32 makes h0, h_out,
+    conv_init and conv_final slot caches indexed per batch row (negative: padding row, y = 0);
+    ``h_all`` (B, L, D, N) fp32 receives the state after every step.  ``workspace`` (uint8 CUDA tensor,
+    optional) enables the L split; pass ``workspace="auto"`` to allocate it here.  Returns y, or
+    (y, h_out) with return_state."""
     if y is None:
         y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
     if return_state and h_out is None:
+        if state_indices is not None:
+            raise ValueError("with state_indices, pass the slot cache as h_out")
         h_out = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
     if isinstance(workspace, str) and workspace == "auto":
         n = ssm_scan_workspace_size(u, delta, A, Bm, Cm, Dskip=Dskip, delta_bias=delta_bias, z=z, conv_w=conv_w,
                                     conv_b=conv_b, h0=h0, h_out=h_out, y=y, delta_softplus=delta_softplus, zoh=zoh,
-                                    conv_init=conv_init, conv_final=conv_final)
+                                    conv_init=conv_init, conv_final=conv_final, state_indices=state_indices,
+                                    h_all=h_all)
         workspace = torch.empty(n, dtype=torch.uint8, device=u.device) if n > 0 else None
     p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
-                     workspace, conv_init, conv_final)
+                     workspace, conv_init, conv_final, state_indices, h_all)
     _check(lib().ssm_scan_fwd(ctypes.byref(p), _stream(stream)))
     return (y, h_out) if return_state else y
 
@@ -213,7 +238,8 @@ def ssm_scan_fwd_static(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B
                         h_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
                         delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
                         return_state: bool = False, stream=None, conv_init: Optional[torch.Tensor] = None,
-                        conv_final: Optional[torch.Tensor] = None):
+                        conv_final: Optional[torch.Tensor] = None, state_indices: Optional[torch.Tensor] = None,
+                        h_all: Optional[torch.Tensor] = None):
     """ssm_scan_fwd for callers that cannot allocate scratch: the L split uses the library's fixed
     4 MiB device buffer instead of a workspace.  Calls that may overlap on the GPU share that buffer and
     must be serialised.  Output tensors are allocated here only when not given (pass y / h_out to keep
@@ -223,7 +249,7 @@ def ssm_scan_fwd_static(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B
     if return_state and h_out is None:
         h_out = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
     p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
-                     None, conv_init, conv_final)
+                     None, conv_init, conv_final, state_indices, h_all)
     _check(lib().ssm_scan_fwd_static(ctypes.byref(p), _stream(stream)))
     return (y, h_out) if return_state else y
 
@@ -251,23 +277,27 @@ def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, 
                      delta_bias: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
                      y: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = True,
                      stream=None, conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
-                     conv_state: Optional[torch.Tensor] = None) -> torch.Tensor:
+                     conv_state: Optional[torch.Tensor] = None,
+                     state_indices: Optional[torch.Tensor] = None) -> torch.Tensor:
     """One decode step: state (B, D, N) fp32 updated in place; u/delta/z (B, D), Bm/Cm (B, N).  Returns y (B, D).
     With ``conv_w`` (D, W) fp32 the conv front end is fused (ssm_state_update_conv): u is the conv input x,
-    ``conv_state`` (B, D, W-1) of u's dtype holds the previous W-1 inputs and is updated in place."""
-    Bsz, D, N = state.shape
+    ``conv_state`` (B, D, W-1) of u's dtype holds the previous W-1 inputs and is updated in place.
+    With ``state_indices`` (B,) int32, state and conv_state are slot caches (S, D, N), (S, D, W-1) and
+    batch row b uses slot state_indices[b] (negative: padding row, y = 0)."""
+    _, D, N = state.shape
+    Bsz = u.shape[0]
     dt = u.dtype
     if dt not in _DT:
         raise ValueError(f"unsupported dtype {dt}")
     if y is None:
         y = torch.empty_like(u)
-    if conv_w is not None:
-        if conv_w.dim() != 2 or conv_w.shape[0] != D:
+    if conv_w is not None or state_indices is not None:
+        if conv_w is not None and (conv_w.dim() != 2 or conv_w.shape[0] != D):
             raise ValueError("conv_w must be (dim, width)")
-        W = conv_w.shape[1]
+        W = conv_w.shape[1] if conv_w is not None else 1
         p = StepParams()
         p.batch, p.dim, p.dstate, p.dtype = Bsz, D, N, _DT[dt]
-        p.state = _ptr(state, "state", torch.float32, (Bsz, D, N))
+        p.state = _ptr(state, "state", torch.float32, _slots_shape(state, "state", Bsz, (D, N), state_indices))
         p.x = _ptr(u, "u", dt, (Bsz, D))
         p.delta = _ptr(delta, "delta", dt, (Bsz, D))
         p.A = _ptr(A, "A", torch.float32, (D, N))
@@ -277,15 +307,18 @@ def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, 
         p.delta_bias = _ptr(delta_bias, "delta_bias", torch.float32, (D,))
         p.z = _ptr(z, "z", dt, (Bsz, D))
         p.conv_w = _ptr(conv_w, "conv_w", torch.float32)
-        p.conv_b = _ptr(conv_b, "conv_b", torch.float32, (D,))
+        p.conv_b = _ptr(conv_b, "conv_b", torch.float32, (D,)) if conv_w is not None else None
         p.conv_width = W
-        p.conv_state = _ptr(conv_state, "conv_state", dt, (Bsz, D, W - 1)) if W > 1 else None
+        p.conv_state = (_ptr(conv_state, "conv_state", dt,
+                             _slots_shape(conv_state, "conv_state", Bsz, (D, W - 1), state_indices))
+                        if W > 1 else None)
+        p.state_indices = _ptr(state_indices, "state_indices", torch.int32, (Bsz,))
         p.y = _ptr(y, "y", dt, (Bsz, D))
         p.delta_softplus = int(bool(delta_softplus))
         p.zoh = int(bool(zoh))
         _check(lib().ssm_state_update_conv(ctypes.byref(p), _stream(stream)))
         return y
-    _check(lib().ssm_state_update(_ptr(state, "state", torch.float32), _ptr(u, "u", dt, (Bsz, D)),
+    _check(lib().ssm_state_update(_ptr(state, "state", torch.float32, (Bsz, D, N)), _ptr(u, "u", dt, (Bsz, D)),
                                   _ptr(delta, "delta", dt, (Bsz, D)), _ptr(A, "A", torch.float32, (D, N)),
                                   _ptr(Bm, "Bm", dt, (Bsz, N)), _ptr(Cm, "Cm", dt, (Bsz, N)),
                                   _ptr(Dskip, "Dskip", torch.float32, (D,)),

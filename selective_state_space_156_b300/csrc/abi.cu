@@ -56,6 +56,8 @@ bool aligned_rows(const ssm_scan_params* p) {
 }
 
 int scan_kind(const ssm_scan_params* p) {
+    // state slots and the per-step state output are implemented by the element-wise kernel
+    if (p->state_indices != nullptr || p->h_all != nullptr) return ssm::kScanSeq;
     if (p->in_dtype == SSM_BF16 && p->out_dtype == SSM_BF16 && aligned_rows(p)) {
         if (p->dstate <= 16) return ssm::kScanP16;
         if (p->dstate <= 64) return ssm::kScanG4;
@@ -113,6 +115,15 @@ SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
     return p;
 }
 
+// The plan of one call: state slots are never split (the split's h0 copy is indexed by batch row).
+SegPlan scan_plan(const ssm_scan_params* p, int kind, int lpc) {
+    if (p->state_indices != nullptr) {
+        const int chunk = kind_geom(kind, lpc).chunk;
+        return SegPlan{1, ((p->seqlen + chunk - 1) / chunk) * chunk};
+    }
+    return plan_segments(kind, lpc, p->batch, p->dim, p->seqlen);
+}
+
 size_t workspace_bytes_for(const ssm_scan_params* p, const SegPlan& sp) {
     if (sp.nseg <= 1) return 0;
     const size_t rows = (size_t)p->batch * p->dim;
@@ -143,7 +154,7 @@ ssm_status validate_scan(const ssm_scan_params* p) {
     if (!dstate_supported(p))
         return fail(SSM_ERR_UNSUPPORTED,
                     "ssm_scan_fwd: dstate %d not supported (1..16; 32 and 64 need bf16 in/out, 16-byte-aligned "
-                    "rows and seqlen %% 8 == 0)", p->dstate);
+                    "rows, seqlen %% 8 == 0 and neither state_indices nor h_all)", p->dstate);
     const size_t rows = (size_t)p->batch * p->dim;
     if (rows * (size_t)p->seqlen >= ((size_t)1 << 40))
         return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: batch*dim*seqlen too large");
@@ -157,7 +168,16 @@ ssm_status validate_scan(const ssm_scan_params* p) {
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: y overlaps an input");
     if (p->h_out != nullptr && overlaps(p->h_out, rows * p->dstate * 4, p->y, ybytes))
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_out overlaps y");
-    if (p->conv_w != nullptr && p->conv_width > 1) {
+    if (p->h_all != nullptr) {
+        const size_t hb = nbdl * (size_t)p->dstate * 4;
+        if (overlaps(p->h_all, hb, p->u, nbdl * ib) || overlaps(p->h_all, hb, p->delta, nbdl * ib) ||
+            overlaps(p->h_all, hb, p->z, nbdl * ib) || overlaps(p->h_all, hb, p->Bm, nbnl * ib) ||
+            overlaps(p->h_all, hb, p->Cm, nbnl * ib) || overlaps(p->h_all, hb, p->y, ybytes) ||
+            (p->h_out && !p->state_indices && overlaps(p->h_all, hb, p->h_out, rows * p->dstate * 4)) ||
+            (p->h0 && !p->state_indices && overlaps(p->h_all, hb, p->h0, rows * p->dstate * 4)))
+            return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_all overlaps another tensor");
+    }
+    if (p->conv_w != nullptr && p->conv_width > 1 && p->state_indices == nullptr) {
         const size_t cbytes = rows * (size_t)(p->conv_width - 1) * ib;
         if (p->conv_init != nullptr && (overlaps(p->conv_init, cbytes, p->y, ybytes) ||
                                         (p->h_out && overlaps(p->conv_init, cbytes, p->h_out, rows * p->dstate * 4))))
@@ -185,6 +205,8 @@ ssm::ScanKernelArgs scan_args(const ssm_scan_params* p) {
     a.Dskip = p->Dskip; a.delta_bias = p->delta_bias; a.z = p->z;
     a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
     a.conv_init = (p->conv_w && p->conv_width > 1) ? p->conv_init : nullptr;
+    a.state_indices = p->state_indices;
+    a.h_all = p->h_all;
     a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
     a.softplus = p->delta_softplus;
     a.vec = aligned_rows(p);
@@ -200,8 +222,8 @@ ssm_status launch_scan_and_history(const ssm::ScanKernelArgs& a, const ssm_scan_
     cudaError_t e = ssm::launch_scan(a, (int)p->in_dtype, (int)p->out_dtype, p->zoh, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e, who);
     if (p->conv_w != nullptr && p->conv_width > 1 && p->conv_final != nullptr) {
-        e = ssm::launch_conv_history(p->u, a.conv_init, p->conv_final, (size_t)p->batch * p->dim, p->seqlen,
-                                     p->conv_width - 1, (int)p->in_dtype, (cudaStream_t)stream);
+        e = ssm::launch_conv_history(p->u, a.conv_init, p->conv_final, p->state_indices, p->batch, p->dim,
+                                     p->seqlen, p->conv_width - 1, (int)p->in_dtype, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_status(e, who);
     }
     return SSM_OK;
@@ -262,7 +284,7 @@ ssm_status ssm_device_error(unsigned* flags) {
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     if (validate_scan(p) != SSM_OK) return 0;
-    return workspace_bytes_for(p, plan_segments(scan_kind(p), choose_lpc(p), p->batch, p->dim, p->seqlen));
+    return workspace_bytes_for(p, scan_plan(p, scan_kind(p), choose_lpc(p)));
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
@@ -271,7 +293,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
 
     ssm::ScanKernelArgs a = scan_args(p);
 
-    SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
+    SegPlan sp = scan_plan(p, a.kind, a.lpc);
     const size_t need = workspace_bytes_for(p, sp);
     if (sp.nseg > 1 && (p->workspace == nullptr || p->workspace_bytes < need)) {
         const int chunk = kind_geom(a.kind, a.lpc).chunk;
@@ -329,6 +351,7 @@ ssm_status run_decode_step(const ssm::DecodeStep& st, ssm_dtype dtype, const cha
     }
     const size_t bd = (size_t)st.Bsz * st.D * esize(dtype);
     const size_t bn = (size_t)st.Bsz * st.N * esize(dtype);
+    // with state slots the cache holds an unknown number of slots: its checks below cover one slot per row
     const size_t sb = (size_t)st.Bsz * st.D * st.N * 4;
     const void* y = st.y;
     if (overlaps(y, bd, st.x, bd) || overlaps(y, bd, st.delta, bd) || overlaps(y, bd, st.z, bd) ||
@@ -379,6 +402,7 @@ ssm_status ssm_state_update_conv(const ssm_step_params* p, ssm_stream_t stream) 
         st.conv_width = p->conv_width;
         st.conv_state = p->conv_width > 1 ? p->conv_state : nullptr;
     }
+    st.state_indices = p->state_indices;
     return run_decode_step(st, p->dtype, "ssm_state_update_conv", (cudaStream_t)stream);
 }
 
@@ -389,7 +413,7 @@ ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
     ssm::ScanKernelArgs a = scan_args(p);
 
     // the same launch plan as ssm_scan_fwd with a large enough workspace; p->workspace is ignored
-    const SegPlan sp = plan_segments(a.kind, a.lpc, p->batch, p->dim, p->seqlen);
+    const SegPlan sp = scan_plan(p, a.kind, a.lpc);
     const size_t need = workspace_bytes_for(p, sp);
     if (need > kStaticScratchBytes)
         return fail(SSM_ERR_UNSUPPORTED,

@@ -83,12 +83,16 @@ cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, 
 // (plain loads: the history may be the output buffer) before it writes.
 template <typename T>
 __global__ void __launch_bounds__(kConvThreads) conv_history_kernel(const void* __restrict__ x, const void* conv_init,
-                                                                    void* conv_final, size_t rows, int L, int W1) {
+                                                                    void* conv_final, const int* state_indices, int D,
+                                                                    int L, int W1) {
     using S = typename T::storage;
-    const size_t r = (size_t)blockIdx.x * kConvThreads + threadIdx.x;
-    if (r >= rows) return;
+    const int d = blockIdx.x * kConvThreads + threadIdx.x, b = blockIdx.y;
+    if (d >= D) return;
+    const int slot = state_indices != nullptr ? state_indices[b] : b;
+    if (slot < 0) return;  // a padding row owns no slot
+    const size_t r = (size_t)b * D + d, sr = (size_t)slot * D + d;
     const S* xr = static_cast<const S*>(x) + r * (size_t)L;
-    const S* hi = conv_init != nullptr ? static_cast<const S*>(conv_init) + r * W1 : nullptr;
+    const S* hi = conv_init != nullptr ? static_cast<const S*>(conv_init) + sr * W1 : nullptr;
     S v[3];
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -96,20 +100,20 @@ __global__ void __launch_bounds__(kConvThreads) conv_history_kernel(const void* 
         v[i] = S(0);
         if (i < W1) v[i] = t >= 0 ? xr[t] : (hi != nullptr ? hi[W1 + t] : S(0));
     }
-    S* out = static_cast<S*>(conv_final) + r * W1;
+    S* out = static_cast<S*>(conv_final) + sr * W1;
 #pragma unroll
     for (int i = 0; i < 3; ++i)
         if (i < W1) out[i] = v[i];
 }
 
-cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, size_t rows, int L, int W1,
-                                int dtype, cudaStream_t stream) {
+cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, const int* state_indices,
+                                int Bsz, int D, int L, int W1, int dtype, cudaStream_t stream) {
     if (W1 < 1 || W1 > 3) return cudaErrorInvalidValue;
-    const unsigned grid = (unsigned)((rows + kConvThreads - 1) / kConvThreads);
+    const dim3 grid((unsigned)((D + kConvThreads - 1) / kConvThreads), (unsigned)Bsz);
     if (dtype == 1)
-        conv_history_kernel<BF16><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, rows, L, W1);
+        conv_history_kernel<BF16><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, state_indices, D, L, W1);
     else
-        conv_history_kernel<F32><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, rows, L, W1);
+        conv_history_kernel<F32><<<grid, kConvThreads, 0, stream>>>(x, conv_init, conv_final, state_indices, D, L, W1);
     return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@ struct ChannelConsts {
 template <typename Tin, typename Tout, int NS, Disc kDisc, bool kFinal, bool kTail>
 __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanShared<NS>& sh, int g, size_t rowoff,
                                            int tg, int nv, const ChannelConsts<NS>& cc, float (&h)[NS],
-                                           float (&xh)[3], float& dsum) {
+                                           float (&xh)[3], float& dsum, float* hall) {
     float xv[8], dv[8], zv[8];
     const bool has_z = kFinal && a.z != nullptr;
     if (!kTail) {
@@ -129,6 +129,13 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
             }
         }
         if (kFinal) out[j] = fmaf(cc.dskip, vj, y0 + y1) * gate[j];
+        if (kFinal && hall != nullptr) {
+            // the state after step tg + j: row (b, tg + j, d) of h_all, stride D * N per step
+            float* hp = hall + (size_t)(tg + j) * a.D * a.N;
+#pragma unroll
+            for (int n = 0; n < NS; ++n)
+                if (n < a.N) hp[n] = h[n];
+        }
     }
 
     if (kFinal) {
@@ -145,7 +152,7 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
 template <typename Tin, typename Tout, int NS, Disc kDisc, bool kFinal>
 __device__ __forceinline__ void scan_segment(const ScanKernelArgs& a, ScanShared<NS>& sh, bool active, int b, size_t row,
                                              int t_begin, int t_end, const ChannelConsts<NS>& cc, float (&h)[NS],
-                                             float (&xh)[3], float& dsum) {
+                                             float (&xh)[3], float& dsum, float* hall) {
     const size_t rowoff = row * (size_t)a.L;
     for (int c0 = t_begin; c0 < t_end; c0 += kScanChunk) {
         const int clen = min(kScanChunk, t_end - c0);
@@ -165,9 +172,9 @@ __device__ __forceinline__ void scan_segment(const ScanKernelArgs& a, ScanShared
             for (int g = 0; g < clen; g += 8) {
                 const int nv = min(8, clen - g);
                 if (a.vec && nv == 8)
-                    scan_group<Tin, Tout, NS, kDisc, kFinal, false>(a, sh, g, rowoff, c0 + g, 8, cc, h, xh, dsum);
+                    scan_group<Tin, Tout, NS, kDisc, kFinal, false>(a, sh, g, rowoff, c0 + g, 8, cc, h, xh, dsum, hall);
                 else
-                    scan_group<Tin, Tout, NS, kDisc, kFinal, true>(a, sh, g, rowoff, c0 + g, nv, cc, h, xh, dsum);
+                    scan_group<Tin, Tout, NS, kDisc, kFinal, true>(a, sh, g, rowoff, c0 + g, nv, cc, h, xh, dsum, hall);
             }
         }
     }
@@ -186,6 +193,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
     const size_t row = (size_t)b * a.D + (active ? d : 0);
     const int t_begin = seg * a.seg_len;
     const int t_end = min(a.L, t_begin + a.seg_len);
+    // The row's state slot (state_indices: a cache indexed by request; negative = padding row).  h0,
+    // h_out and conv_init are indexed by it; u, delta, z, y, B, C by the batch row.
+    const int slot = a.state_indices != nullptr ? __ldg(a.state_indices + b) : b;
+    const bool pad = slot < 0;
+    const size_t srow = (size_t)(pad ? 0 : slot) * a.D + (active ? d : 0);
+    float* hall = (kFinal && a.h_all != nullptr && active && !pad) ? a.h_all + ((size_t)b * a.L * a.D + d) * a.N
+                                                                  : nullptr;
 
     ChannelConsts<NS> cc;
     bool has_zero = false;
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
         for (int k = 0; k < 3; ++k) {
             const int t = t_begin - 3 + k;
             if (t >= 0) xh[k] = load1<Tin>(a.u, rowoff + t);
-            else if (a.conv_init != nullptr && t >= -W1) xh[k] = load1<Tin>(a.conv_init, row * W1 + W1 + t);
+            else if (a.conv_init != nullptr && t >= -W1 && !pad) xh[k] = load1<Tin>(a.conv_init, srow * W1 + W1 + t);
         }
     }
 
@@ -231,10 +245,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
 
     if (kFinal) {
         const float* h0 = (a.nseg > 1) ? a.ws_h0 : a.h0;
-        if (h0 != nullptr && active) {
+        const size_t h0row = (a.nseg > 1) ? row : srow;  // the L split is never planned with state slots
+        if (h0 != nullptr && active && !pad) {
 #pragma unroll
             for (int n = 0; n < NS; ++n)
-                if (n < a.N) h[n] = h0[row * a.N + n];
+                if (n < a.N) h[n] = h0[h0row * a.N + n];
         }
         // Fold in the summaries of the earlier segments.
         for (int s = 0; s < seg; ++s) {
@@ -253,17 +268,24 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
     }
 
     constexpr Disc kMain = kZOH ? Disc::kZOH : Disc::kSimple;
+    const bool run = active && !pad;
     if (kZOH && __any_sync(0xffffffffu, has_zero))
-        scan_segment<Tin, Tout, NS, Disc::kZOHSafe, kFinal>(a, sh, active, b, row, t_begin, t_end, cc, h, xh, dsum);
+        scan_segment<Tin, Tout, NS, Disc::kZOHSafe, kFinal>(a, sh, run, b, row, t_begin, t_end, cc, h, xh, dsum, hall);
     else
-        scan_segment<Tin, Tout, NS, kMain, kFinal>(a, sh, active, b, row, t_begin, t_end, cc, h, xh, dsum);
+        scan_segment<Tin, Tout, NS, kMain, kFinal>(a, sh, run, b, row, t_begin, t_end, cc, h, xh, dsum, hall);
 
     if (!active) return;
+    if (pad) {  // a padding row: y is zero, no slot is touched
+        if (kFinal)
+            for (int t = t_begin; t < t_end; ++t) store1<Tout>(a.y, row * (size_t)a.L + t, 0.0f);
+        return;
+    }
     if (kFinal) {
         if (seg == a.nseg - 1 && a.h_out != nullptr) {
+            const size_t orow = (a.nseg > 1) ? row : srow;
 #pragma unroll
             for (int n = 0; n < NS; ++n)
-                if (n < a.N) a.h_out[row * a.N + n] = h[n];
+                if (n < a.N) a.h_out[orow * a.N + n] = h[n];
         }
     } else {
         a.ws_dsum[(size_t)seg * rows + row] = dsum;

@@ -24,7 +24,9 @@ struct ScanKernelArgs {
     const float* conv_w;
     const float* conv_b;
     int conv_width;
-    const void* conv_init;  // (B*D, conv_width - 1) x before t = 0 (in dtype), or NULL for zeros
+    const void* conv_init;  // (rows, conv_width - 1) x before t = 0 (in dtype), or NULL for zeros
+    const int* state_indices;  // (B) slot of each batch row in h0 / h_out / conv_init, or NULL (slot = b)
+    float* h_all;              // (B, L, D, N) state after every step, or NULL
     const float* h0;
     float* h_out;
     void* y;
@@ -49,10 +51,10 @@ constexpr int kScanChunk = 64;     // timesteps of B/C staged in shared memory a
 // Launches the summary (when nseg > 1) and final scan kernels.  in/out: 0 = f32, 1 = bf16.
 cudaError_t launch_scan(const ScanKernelArgs& a, int in_dtype, int out_dtype, int zoh, cudaStream_t stream);
 
-// conv_final[r, i] = x_{L - W1 + i} of row r (from conv_init where that time is negative, zero without
-// it), W1 = conv_width - 1, for rows * W1 elements; conv_final may be conv_init itself.
-cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, size_t rows, int L, int W1,
-                                int dtype, cudaStream_t stream);
+// conv_final[s, i] = x_{L - W1 + i} of the batch row whose slot is s (from conv_init where that time is
+// negative, zero without it), W1 = conv_width - 1; conv_final may be conv_init itself.
+cudaError_t launch_conv_history(const void* x, const void* conv_init, void* conv_final, const int* state_indices,
+                                int Bsz, int D, int L, int W1, int dtype, cudaStream_t stream);
 
 cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* b, void* y, int Bsz, int D, int L,
                                  int width, int silu, int dtype, cudaStream_t stream);
@@ -73,6 +75,7 @@ struct DecodeStep {
     const float* conv_b;  // (D) or NULL
     void* conv_state;     // (B, D, conv_width - 1) or NULL (conv_width == 1)
     int conv_width;
+    const int* state_indices;  // (B) slot of each batch row in state / conv_state, or NULL (slot = b)
     int Bsz, D, N, softplus, zoh, dtype;  // dtype: 0 = f32, 1 = bf16
 };
 

@@ -55,7 +55,14 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
     const int d = blockIdx.x * (kDecThreads / kDecLanes) + threadIdx.x / kDecLanes;
     const bool active = d < D;
     const int b = blockIdx.y;
-    const size_t row = (size_t)b * D + (active ? d : 0);
+    const size_t row = (size_t)b * D + (active ? d : 0);  // u, delta, z, y
+    // the row's slot in the state cache (state_indices), negative for a padding row
+    const int slot = s.state_indices != nullptr ? __ldg(s.state_indices + b) : b;
+    if (slot < 0) {
+        if (active && e == 0) store1<T>(s.y, row, 0.0f);
+        return;  // uniform over the row's lanes: no shuffle is left half-done
+    }
+    const size_t srow = (size_t)slot * D + (active ? d : 0);  // state, conv_state
 
     // issue every load first: the state (the HBM stream), then the L2-resident operands
     float h[NSL], av[NSL], Bt[NSL], Ct[NSL];
@@ -64,11 +71,11 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
         const int n0 = 4 * kDecLanes * k + 4 * e;
         const bool full = vec && active && n0 + 3 < N;
         if (full) {
-            const float4 w = __ldcs(reinterpret_cast<const float4*>(state + row * N + n0));
+            const float4 w = __ldcs(reinterpret_cast<const float4*>(state + srow * N + n0));
             h[4 * k] = w.x; h[4 * k + 1] = w.y; h[4 * k + 2] = w.z; h[4 * k + 3] = w.w;
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) h[4 * k + i] = (active && n0 + i < N) ? state[row * N + n0 + i] : 0.0f;
+            for (int i = 0; i < 4; ++i) h[4 * k + i] = (active && n0 + i < N) ? state[srow * N + n0 + i] : 0.0f;
         }
         float t4[4];
         if (full) {
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
         // first); both lanes of the row read the state before lane 0 writes the shifted one back
         using Sx = typename T::storage;
         const int W = s.conv_width, W1 = W - 1;
-        Sx* cs = static_cast<Sx*>(s.conv_state) + row * W1;
+        Sx* cs = static_cast<Sx*>(s.conv_state) + srow * W1;
         float c = (s.conv_b != nullptr && active) ? __ldg(s.conv_b + d) : 0.0f;
         Sx hist[3];
 #pragma unroll
@@ -156,12 +163,12 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
     for (int k = 0; k < NSL / 4; ++k) {
         const int n0 = 4 * kDecLanes * k + 4 * e;
         if (vec && n0 + 3 < N) {
-            __stcs(reinterpret_cast<float4*>(state + row * N + n0),
+            __stcs(reinterpret_cast<float4*>(state + srow * N + n0),
                    make_float4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]));
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (n0 + i < N) state[row * N + n0 + i] = h[4 * k + i];
+                if (n0 + i < N) state[srow * N + n0 + i] = h[4 * k + i];
         }
     }
 }

@@ -78,6 +78,7 @@ struct DecodeArgs {
     const float* conv_b;  // (D) or NULL
     void* conv_state;     // (B, D, W - 1), read and written; NULL when W == 1
     int W;
+    const int* state_indices;  // (B) slot of each batch row in state / conv_state, or NULL (slot = b)
     int Bsz, D, softplus;
 };
 
@@ -150,6 +151,12 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                 const size_t r0 = (size_t)b * a.D + d0;
                 uint64_t* bar = &full[s];
                 unsigned char* st = stages + s * L::kBytes;
+                const int slot = a.state_indices != nullptr ? __ldg(a.state_indices + b) : b;
+                if (slot < 0) {  // a padding row: nothing to copy, the stage is complete at once
+                    mbar_arrive(bar);
+                    continue;
+                }
+                const size_t s0 = (size_t)slot * a.D + d0;  // the tile's first row in the state cache
                 const unsigned sb = (unsigned)(rows * N * 4), eb = (unsigned)(rows * E), pb = (unsigned)(rows * 4);
                 unsigned bytes = 2 * sb + 2 * eb + (a.z ? eb : 0u) + 2u * N * E + (a.Dskip ? pb : 0u) +
                                  (a.delta_bias ? pb : 0u);
@@ -158,12 +165,12 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                 mbar_arrive_expect_tx(bar, bytes);
                 if (kConv) {
                     if (a.W > 1)
-                        bulk_g2s(st + L::kOffCS, static_cast<const unsigned char*>(a.conv_state) + r0 * (a.W - 1) * E,
+                        bulk_g2s(st + L::kOffCS, static_cast<const unsigned char*>(a.conv_state) + s0 * (a.W - 1) * E,
                                  csb, bar);
                     bulk_g2s(st + L::kOffCW, a.conv_w + (size_t)d0 * a.W, cwb, bar);
                     if (a.conv_b) bulk_g2s(st + L::kOffCB, a.conv_b + d0, pb, bar);
                 }
-                bulk_g2s(st + L::kOffState, a.state + r0 * N, sb, bar);
+                bulk_g2s(st + L::kOffState, a.state + s0 * N, sb, bar);
                 bulk_g2s(st + L::kOffA, a.A + (size_t)d0 * N, sb, bar);
                 bulk_g2s(st + L::kOffU, static_cast<const unsigned char*>(a.u) + r0 * E, eb, bar);
                 bulk_g2s(st + L::kOffDt, static_cast<const unsigned char*>(a.delta) + r0 * E, eb, bar);
@@ -189,6 +196,15 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
             const int d0 = (t - b * tiles_per_b) * kTileRows;
             const int rows = min(kTileRows, a.D - d0);
             const size_t r0 = (size_t)b * a.D + d0;
+            const int slot = a.state_indices != nullptr ? __ldg(a.state_indices + b) : b;
+            if (slot < 0) {  // a padding row: y = 0, no slot touched
+                for (int r = tid / TPR; r < rows; r += RPP)
+                    if (q == 0) store1<T>(a.y, r0 + r, 0.0f);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                continue;
+            }
+            const size_t s0 = (size_t)slot * a.D + d0;
             const unsigned char* st = stages + s * L::kBytes;
             const float* hs = reinterpret_cast<const float*>(st + L::kOffState);
             const float* As = reinterpret_cast<const float*>(st + L::kOffA);
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                         // the new conv state: the last W - 1 inputs, oldest first (raw values, no rounding)
                         using Sx = typename T::storage;
                         const Sx* cs = reinterpret_cast<const Sx*>(st + L::kOffCS) + r * W1;
-                        Sx* out = static_cast<Sx*>(a.conv_state) + (r0 + r) * W1;
+                        Sx* out = static_cast<Sx*>(a.conv_state) + (s0 + r) * W1;
 #pragma unroll
                         for (int k = 0; k < 3; ++k)
                             if (k < W1) out[k] = k + 1 < W1 ? cs[k + 1] : reinterpret_cast<const Sx*>(st + L::kOffU)[r];
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                 if (r < rows) {
 #pragma unroll
                     for (int c = 0; c < SL / 4; ++c)
-                        __stcs(reinterpret_cast<float4*>(a.state + (r0 + r) * N + SL * q + 4 * c),
+                        __stcs(reinterpret_cast<float4*>(a.state + (s0 + r) * N + SL * q + 4 * c),
                                make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]));
                     if (q == 0) store1<T>(a.y, r0 + r, fmaf(dsk, uv, yp) * gate);
                 }
@@ -341,7 +357,7 @@ bool state_update_bulk_eligible(const DecodeStep& s) {
 cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream) {
     const DecodeArgs a{s.state, s.x, s.delta, s.A, s.Bm, s.Cm, s.Dskip, s.delta_bias, s.z, s.y,
                        s.conv_w, s.conv_w ? s.conv_b : nullptr, s.conv_w ? s.conv_state : nullptr,
-                       s.conv_w ? s.conv_width : 1, s.Bsz, s.D, s.softplus};
+                       s.conv_w ? s.conv_width : 1, s.state_indices, s.Bsz, s.D, s.softplus};
     if (s.dtype == 1) return launch_bulk_t<BF16>(a, s.N, s.zoh, stream);
     return launch_bulk_t<F32>(a, s.N, s.zoh, stream);
 }

@@ -75,7 +75,7 @@ def test_params_struct_layout_matches_c():
     got = _c_layout("ssm_scan_params", """
   F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(out_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip)
   F(delta_bias) F(z) F(conv_w) F(conv_b) F(conv_width) F(h0) F(h_out) F(y) F(delta_softplus) F(zoh)
-  F(workspace) F(workspace_bytes) F(conv_init) F(conv_final)""")
+  F(workspace) F(workspace_bytes) F(conv_init) F(conv_final) F(state_indices) F(h_all)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanParams)
     assert len(got) == len(ssm.ScanParams._fields_)
     for name, off in got.items():
@@ -85,7 +85,7 @@ def test_params_struct_layout_matches_c():
 def test_step_params_struct_layout_matches_c():
     got = _c_layout("ssm_step_params", """
   F(batch) F(dim) F(dstate) F(dtype) F(state) F(x) F(delta) F(A) F(Bm) F(Cm) F(Dskip) F(delta_bias) F(z)
-  F(conv_w) F(conv_b) F(conv_width) F(conv_state) F(y) F(delta_softplus) F(zoh)""")
+  F(conv_w) F(conv_b) F(conv_width) F(conv_state) F(y) F(delta_softplus) F(zoh) F(state_indices)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.StepParams)
     assert len(got) == len(ssm.StepParams._fields_)
     for name, off in got.items():
