@@ -1,5 +1,7 @@
 """CPU fp64 oracle for the selective scan -- TEST INFRASTRUCTURE ONLY.
 
+(The backward pass's oracle is ``oracle.backward``: autograd of the same recurrence in fp64 torch ops.)
+
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import
 this package.  The product path (``selective_state_space_156_b300``) never imports it and
 shares no code with it: the arithmetic lives in ``oracle.c`` (plain C, fp64, libm), this

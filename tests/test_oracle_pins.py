@@ -496,3 +496,49 @@ def test_threads_do_not_change_results():
     assert n1 == 1
     np.testing.assert_array_equal(y1, y8)
     np.testing.assert_array_equal(h1, h8)
+
+
+# ---------------------------------------------------------------------------------------------
+# Backward oracle (autograd of a plain fp64 torch recurrence) against central finite differences of
+# the C forward oracle: d/dp of sum(y * dy) + sum(h_L * dh) for every input p, at sampled coordinates
+# ---------------------------------------------------------------------------------------------
+def _objective(d, dy, dh):
+    y, h, _ = oracle.scan(d, nthreads=1)
+    Bsz, D, L = d["u"].shape
+    return float((y.reshape(Bsz, D, L) * dy).sum() + (h.reshape(dh.shape) * dh).sum())
+
+
+@pytest.mark.parametrize("zoh,conv,softplus", [(True, True, True), (False, False, True), (True, False, False)])
+def test_backward_oracle_matches_finite_differences(zoh, conv, softplus):
+    from oracle import backward as bwd
+    Bsz, D, N, L = 2, 3, 4, 7
+    d = _inputs(Bsz, D, N, L, zoh=zoh, with_z=True, conv=conv, h0=True, seed=200 + int(zoh) + 2 * int(conv),
+                delta_softplus=softplus)
+    d["A"][1, 2] = 0.0  # the a -> 0 limit and its derivative
+    if not softplus:  # dt = delta + bias directly: keep it positive, as a step size is
+        d["delta"] = 0.02 + 0.1 * d["delta"].abs()
+        d["delta_bias"] = torch.full((D,), 0.01, dtype=torch.float64)
+    if conv:
+        d["conv_init"] = torch.tensor(np.random.default_rng(5).standard_normal((Bsz, D, 3)))
+    g = np.random.default_rng(21)
+    dy = g.standard_normal((Bsz, D, L))
+    dh = g.standard_normal((Bsz, D, N))
+    grads = bwd.scan_bwd(d, dy, dh)
+    y_ref, _, _ = oracle.scan(d, nthreads=1)
+    np.testing.assert_allclose(grads["y"].reshape(-1, L), y_ref, rtol=1e-12, atol=1e-13)
+    keys = ["u", "delta", "A", "Bm", "Cm", "Dskip", "delta_bias", "z", "h0"] + (["conv_w", "conv_b", "conv_init"]
+                                                                                if conv else [])
+    eps = 1e-6
+    for k in keys:
+        base = d[k]
+        flat = base.reshape(-1)
+        for i in g.choice(flat.numel(), size=min(6, flat.numel()), replace=False):
+            orig = float(flat[i])
+            flat[i] = orig + eps
+            fp = _objective(d, dy, dh)
+            flat[i] = orig - eps
+            fm = _objective(d, dy, dh)
+            flat[i] = orig
+            fd = (fp - fm) / (2 * eps)
+            got = grads[k].reshape(-1)[i]
+            assert abs(got - fd) <= 1e-6 * (1.0 + abs(fd)), (k, int(i), got, fd)
