@@ -194,6 +194,62 @@ SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *del
                             ssm_stream_t stream);
 
 /*
+ * Backward pass of the selective scan (training; pwwt.cn/news/5168881 section 3.2): the gradients of
+ * sum(y * dy) + sum(h_L * dh_out) with respect to every input of the forward call.
+ *
+ * Forward inputs (batch, dim, dstate, seqlen, in_dtype, u, delta, A, Bm, Cm, Dskip, delta_bias, z,
+ * conv_w, conv_b, conv_width, conv_init, h0, delta_softplus, zoh) are exactly those of the forward
+ * call, and
+ *   h_all    (B, L, D, N) float32  the forward's state after every step (ssm_scan_fwd with h_all)  required
+ *   dy       (B, D, L) in_dtype    gradient of y                                                  required
+ *   dh_out   (B, D, N) float32     gradient of the final state, or NULL for zero
+ * Outputs (element-wise ones in in_dtype, the rest float32; each may be NULL only where its input was):
+ *   du, ddelta (B, D, L)           required (du is the gradient of x when the conv is fused)
+ *   dz (B, D, L)                   required with z
+ *   dA (D, N); dB, dC (B, N, L)    required
+ *   dDskip, ddelta_bias (D); dconv_w (D, W); dconv_b (D); dconv_init (B, D, W-1); dh0 (B, D, N)
+ * dA, dB, dC, dDskip, ddelta_bias, dconv_w and dconv_b are sums over rows and steps: the call zeroes
+ * them on `stream` and accumulates.  The outputs must not overlap each other or any input.
+ * dstate 1..16.  Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA.
+ */
+typedef struct ssm_scan_bwd_params {
+    int batch, dim, dstate, seqlen;
+    ssm_dtype in_dtype;
+    const void *u;
+    const void *delta;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *Dskip;
+    const float *delta_bias;
+    const void *z;
+    const float *conv_w;
+    const float *conv_b;
+    int conv_width;
+    const void *conv_init;
+    const float *h0;
+    int delta_softplus;
+    int zoh;
+    const float *h_all;
+    const void *dy;
+    const float *dh_out;
+    void *du;
+    void *ddelta;
+    void *dz;
+    float *dA;
+    float *dB;
+    float *dC;
+    float *dDskip;
+    float *ddelta_bias;
+    float *dconv_w;
+    float *dconv_b;
+    void *dconv_init;
+    float *dh0;
+} ssm_scan_bwd_params;
+
+SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream);
+
+/*
  * Device-side failures that a kernel could only record, not return.  (No counterpart on the pages.)
  * The streamed decode kernel bounds every wait for its own bulk copies to about one second; on a
  * timeout it sets a bit in a per-device flag, lets its copies still in flight land (again bounded) and

@@ -50,6 +50,23 @@ class ScanParams(ctypes.Structure):
     ]
 
 
+class ScanBwdParams(ctypes.Structure):
+    """Mirror of ssm_scan_bwd_params in include/ssm_scan.h (same field order and types)."""
+    _fields_ = [
+        ("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int), ("seqlen", ctypes.c_int),
+        ("in_dtype", ctypes.c_int),
+        ("u", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("A", ctypes.c_void_p), ("Bm", ctypes.c_void_p),
+        ("Cm", ctypes.c_void_p), ("Dskip", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("conv_width", ctypes.c_int),
+        ("conv_init", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
+        ("zoh", ctypes.c_int), ("h_all", ctypes.c_void_p), ("dy", ctypes.c_void_p), ("dh_out", ctypes.c_void_p),
+        ("du", ctypes.c_void_p), ("ddelta", ctypes.c_void_p), ("dz", ctypes.c_void_p), ("dA", ctypes.c_void_p),
+        ("dB", ctypes.c_void_p), ("dC", ctypes.c_void_p), ("dDskip", ctypes.c_void_p),
+        ("ddelta_bias", ctypes.c_void_p), ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p),
+        ("dconv_init", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
+    ]
+
+
 class StepParams(ctypes.Structure):
     """Mirror of ssm_step_params in include/ssm_scan.h (same field order and types)."""
     _fields_ = [
@@ -85,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
         L.ssm_state_update.restype = st
         L.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        L.ssm_scan_bwd.restype = st
+        L.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), vp]
         L.ssm_state_update_conv.restype = st
         L.ssm_state_update_conv.argtypes = [ctypes.POINTER(StepParams), vp]
         L.ssm_device_error.restype = st
@@ -334,3 +353,67 @@ def ssm_device_error() -> int:
     flags = ctypes.c_uint(0)
     _check(lib().ssm_device_error(ctypes.byref(flags)))
     return int(flags.value)
+
+
+def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
+                 dy: torch.Tensor, h_all: torch.Tensor, Dskip: Optional[torch.Tensor] = None,
+                 delta_bias: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                 conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
+                 conv_init: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
+                 dh_out: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = True,
+                 stream=None) -> dict:
+    """Backward pass of ssm_scan_fwd: gradients of sum(y * dy) + sum(h_L * dh_out) for every input, keyed
+    like the inputs (``u`` is the gradient of x with a conv; ``h0`` that of the initial state).  ``h_all``
+    (B, L, D, N) fp32 is the forward call's state after every step (ssm_scan_fwd with h_all=...)."""
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    Bsz, D, L = u.shape
+    N = A.shape[1]
+    idt = u.dtype
+    if idt not in _DT:
+        raise ValueError(f"unsupported dtype {idt}")
+    dev = u.device
+    g = {
+        "u": torch.empty_like(u), "delta": torch.empty_like(u), "z": torch.empty_like(u) if z is not None else None,
+        "A": torch.empty((D, N), dtype=torch.float32, device=dev),
+        "Bm": torch.empty((Bsz, N, L), dtype=torch.float32, device=dev),
+        "Cm": torch.empty((Bsz, N, L), dtype=torch.float32, device=dev),
+        "Dskip": torch.empty(D, dtype=torch.float32, device=dev) if Dskip is not None else None,
+        "delta_bias": torch.empty(D, dtype=torch.float32, device=dev) if delta_bias is not None else None,
+        "conv_w": torch.empty_like(conv_w) if conv_w is not None else None,
+        "conv_b": torch.empty(D, dtype=torch.float32, device=dev) if (conv_w is not None and conv_b is not None)
+        else None,
+        "conv_init": (torch.empty((Bsz, D, conv_w.shape[1] - 1), dtype=idt, device=dev)
+                      if (conv_w is not None and conv_w.shape[1] > 1) else None),
+        "h0": torch.empty((Bsz, D, N), dtype=torch.float32, device=dev),
+    }
+    p = ScanBwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen = Bsz, D, N, L
+    p.in_dtype = _DT[idt]
+    p.u = _ptr(u, "u", idt)
+    p.delta = _ptr(delta, "delta", idt, (Bsz, D, L))
+    p.A = _ptr(A, "A", torch.float32, (D, N))
+    p.Bm = _ptr(Bm, "Bm", idt, (Bsz, N, L))
+    p.Cm = _ptr(Cm, "Cm", idt, (Bsz, N, L))
+    p.Dskip = _ptr(Dskip, "Dskip", torch.float32, (D,))
+    p.delta_bias = _ptr(delta_bias, "delta_bias", torch.float32, (D,))
+    p.z = _ptr(z, "z", idt, (Bsz, D, L))
+    if conv_w is not None:
+        p.conv_w = _ptr(conv_w, "conv_w", torch.float32)
+        p.conv_b = _ptr(conv_b, "conv_b", torch.float32, (D,))
+        p.conv_width = conv_w.shape[1]
+        if conv_w.shape[1] > 1:
+            p.conv_init = _ptr(conv_init, "conv_init", idt, (Bsz, D, conv_w.shape[1] - 1))
+    p.h0 = _ptr(h0, "h0", torch.float32, (Bsz, D, N))
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    p.h_all = _ptr(h_all, "h_all", torch.float32, (Bsz, L, D, N))
+    p.dy = _ptr(dy, "dy", idt, (Bsz, D, L))
+    p.dh_out = _ptr(dh_out, "dh_out", torch.float32, (Bsz, D, N))
+    p.du, p.ddelta, p.dz = _ptr(g["u"], "du"), _ptr(g["delta"], "ddelta"), _ptr(g["z"], "dz")
+    p.dA, p.dB, p.dC = _ptr(g["A"], "dA"), _ptr(g["Bm"], "dB"), _ptr(g["Cm"], "dC")
+    p.dDskip, p.ddelta_bias = _ptr(g["Dskip"], "dDskip"), _ptr(g["delta_bias"], "ddelta_bias")
+    p.dconv_w, p.dconv_b = _ptr(g["conv_w"], "dconv_w"), _ptr(g["conv_b"], "dconv_b")
+    p.dconv_init, p.dh0 = _ptr(g["conv_init"], "dconv_init"), _ptr(g["h0"], "dh0")
+    _check(lib().ssm_scan_bwd(ctypes.byref(p), _stream(stream)))
+    return {k: v for k, v in g.items() if v is not None}

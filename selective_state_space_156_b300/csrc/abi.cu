@@ -275,6 +275,74 @@ const char* ssm_last_error(void) { return g_last_error.c_str(); }
 
 const char* ssm_version(void) { return "ssm_b300 0.1 (sm_103a)"; }
 
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
+    const char* who = "ssm_scan_bwd";
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "%s: params is NULL", who);
+    if (p->batch <= 0 || p->dim <= 0 || p->dstate <= 0 || p->seqlen <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: sizes must be positive", who);
+    if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "%s: batch %d exceeds 65535", who, p->batch);
+    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "%s: dstate %d not supported (1..16)", who, p->dstate);
+    if (p->in_dtype != SSM_F32 && p->in_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->zoh != 0 && p->zoh != 1))
+        return fail(SSM_ERR_INVALID_ARG, "%s: delta_softplus and zoh must be 0 or 1", who);
+    if (!p->u || !p->delta || !p->A || !p->Bm || !p->Cm || !p->h_all || !p->dy || !p->du || !p->ddelta || !p->dA ||
+        !p->dB || !p->dC)
+        return fail(SSM_ERR_INVALID_ARG, "%s: u, delta, A, Bm, Cm, h_all, dy, du, ddelta, dA, dB and dC are required",
+                    who);
+    if (p->z && !p->dz) return fail(SSM_ERR_INVALID_ARG, "%s: dz is required with z", who);
+    if (p->conv_w && (p->conv_width < 1 || p->conv_width > 4))
+        return fail(SSM_ERR_INVALID_ARG, "%s: conv_width %d outside 1..4", who, p->conv_width);
+    const size_t rows = (size_t)p->batch * p->dim, nbdl = rows * p->seqlen;
+    const size_t eb = esize(p->in_dtype);
+    const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
+    struct Range { const void* p; size_t n; };
+    const Range ins[] = {{p->u, nbdl * eb}, {p->delta, nbdl * eb}, {p->z, nbdl * eb}, {p->Bm, nbnl * eb},
+                         {p->Cm, nbnl * eb}, {p->dy, nbdl * eb}, {p->h_all, nbdl * p->dstate * 4},
+                         {p->A, (size_t)p->dim * p->dstate * 4}, {p->h0, rows * p->dstate * 4}};
+    const Range outs[] = {{p->du, nbdl * eb}, {p->ddelta, nbdl * eb}, {p->dz, nbdl * eb},
+                          {p->dA, (size_t)p->dim * p->dstate * 4}, {p->dB, nbnl * 4}, {p->dC, nbnl * 4},
+                          {p->dDskip, (size_t)p->dim * 4}, {p->ddelta_bias, (size_t)p->dim * 4},
+                          {p->dconv_w, (size_t)p->dim * 4 * 4}, {p->dconv_b, (size_t)p->dim * 4},
+                          {p->dh0, rows * p->dstate * 4}};
+    for (const Range& o : outs) {
+        if (!o.p) continue;
+        for (const Range& i : ins)
+            if (overlaps(o.p, o.n, i.p, i.n)) return fail(SSM_ERR_INVALID_ARG, "%s: an output overlaps an input", who);
+        for (const Range& q : outs)
+            if (&q != &o && overlaps(o.p, o.n, q.p, q.n))
+                return fail(SSM_ERR_INVALID_ARG, "%s: two outputs overlap", who);
+    }
+    ssm::ScanBwdArgs a{};
+    a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
+    a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm; a.Dskip = p->Dskip;
+    a.delta_bias = p->delta_bias; a.z = p->z; a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr;
+    a.conv_width = p->conv_w ? p->conv_width : 0;
+    a.conv_init = (p->conv_w && p->conv_width > 1) ? p->conv_init : nullptr;
+    a.h0 = p->h0; a.h_all = p->h_all; a.dy = p->dy; a.dh_out = p->dh_out;
+    a.du = p->du; a.ddelta = p->ddelta; a.dz = p->z ? p->dz : nullptr; a.dA = p->dA; a.dB = p->dB; a.dC = p->dC;
+    a.dDskip = p->Dskip ? p->dDskip : nullptr; a.ddelta_bias = p->delta_bias ? p->ddelta_bias : nullptr;
+    a.dconv_w = p->conv_w ? p->dconv_w : nullptr; a.dconv_b = (p->conv_w && p->conv_b) ? p->dconv_b : nullptr;
+    a.dconv_init = (p->conv_w && p->conv_width > 1) ? p->dconv_init : nullptr;
+    a.dh0 = p->dh0;
+    a.softplus = p->delta_softplus;
+    const bool a16 = ((size_t)p->seqlen * eb) % 16 == 0 && aligned16(p->u) && aligned16(p->delta) &&
+                     aligned16(p->dy) && aligned16(p->du) && aligned16(p->ddelta) && (!p->z || aligned16(p->z)) &&
+                     (!p->z || aligned16(p->dz)) && p->seqlen % 8 == 0;
+    a.vec = a16 ? 1 : 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the accumulated outputs start from zero
+    const Range acc[] = {{a.dA, (size_t)p->dim * p->dstate * 4}, {a.dB, nbnl * 4}, {a.dC, nbnl * 4},
+                         {a.dDskip, (size_t)p->dim * 4}, {a.ddelta_bias, (size_t)p->dim * 4},
+                         {a.dconv_w, (size_t)p->dim * (p->conv_w ? p->conv_width : 0) * 4},
+                         {a.dconv_b, (size_t)p->dim * 4}};
+    for (const Range& r : acc) {
+        if (!r.p || r.n == 0) continue;
+        cudaError_t e = cudaMemsetAsync(const_cast<void*>(r.p), 0, r.n, st);
+        if (e != cudaSuccess) return cuda_status(e, who);
+    }
+    return cuda_status(ssm::launch_scan_bwd(a, (int)p->in_dtype, p->zoh, st), who);
+}
+
 ssm_status ssm_device_error(unsigned* flags) {
     if (flags == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_device_error: flags is NULL");
     cudaError_t e = cudaDeviceSynchronize();

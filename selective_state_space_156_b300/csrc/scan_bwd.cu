@@ -1,0 +1,344 @@
+// Backward pass of the selective scan (training; pwwt.cn/news/5168881 section 3.2: the gradient runs
+// back along time through the state recurrence).  One thread per (b, d) row, all N states and their
+// adjoints in registers, walking time in reverse:
+//
+//   forward (per step t, state n):  x = dt a,  Abar = e^x,  E = (Abar - 1) / a  (ZOH; dt when a = 0)
+//                                   or E = dt (simplified),  h_t = Abar h_{t-1} + E B v,
+//                                   y_t = (sum_n C h_t + D v) SiLU(z)
+//   backward:  g_n (adjoint of h_t) += C dyss;  dC += dyss h_t;  dAbar = g h_{t-1};  dBbar = g v;
+//              dv += g E B;  dB += dBbar E;  dE = dBbar B;
+//              d(dt) += dAbar Abar a + dE dE/d(dt);  da += dAbar Abar dt + dE dE/da;  g <- Abar g
+//   with dE/d(dt) = Abar, dE/da = (dt Abar - E) / a (dt^2 / 2 at a = 0) for ZOH; 1 and 0 simplified.
+//
+// The states h_t come from the forward call's h_all (the state after every step, (B, L, D, N)): thread
+// (b, d) reads 64 contiguous bytes per step, consecutive threads consecutive rows.  Everything else (conv
+// front end, dt, Abar, E) is recomputed from the inputs.  dB and dC are sums over the channels of a batch
+// row: per step each warp transposes its lanes' contributions through shared memory and sums them, and
+// after a group of 8 steps the block adds its four warp sums to global memory with one atomic per (b, n,
+// t).  Per-channel parameter gradients (dA, D skip, dt bias, conv taps and bias) accumulate over time in
+// registers and are added atomically over the batch at the end; the host zeroes them first.
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kBwdThreads = 128;
+constexpr int kBwdChunk = 64;   // steps of B / C staged per chunk
+constexpr int kBwdGroup = 8;    // steps per group (vector loads / stores, one reduction flush)
+
+template <int NS>
+struct BwdShared {
+    float bc[2][kBwdChunk][NS];               // B_t[n], C_t[n] of the chunk, fp32
+    float tr[kBwdThreads / 32][32][33];       // per-warp transpose of 32 values x 32 lanes (padded)
+    float ws[kBwdThreads / 32][kBwdGroup][32];  // per-warp sums of the group's steps
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + ex2(-x * kLog2e)); }
+
+template <typename T>
+__device__ __forceinline__ float ld(const void* p, size_t i, bool ok) {
+    return ok ? load1<T>(p, i) : 0.0f;
+}
+
+template <typename Tin, int NS, bool kZOH, bool kConv>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs a) {
+    __shared__ BwdShared<NS> sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.y;
+    const int d = blockIdx.x * kBwdThreads + tid;
+    const bool active = d < a.D;
+    const int dd = active ? d : 0;
+    const size_t row = (size_t)b * a.D + dd;
+    const size_t rowoff = row * (size_t)a.L;
+    const int L = a.L, N = a.N;
+
+    // per-channel constants
+    float av[NS], inva[NS];
+#pragma unroll
+    for (int n = 0; n < NS; ++n) {
+        av[n] = (active && n < N) ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
+        inva[n] = av[n] != 0.0f ? 1.0f / av[n] : 0.0f;
+    }
+    float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
+    if (kConv && active) {
+        const int W = a.conv_width;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = i >= 4 - W ? __ldg(a.conv_w + (size_t)dd * W + i - (4 - W)) : 0.0f;
+        if (a.conv_b) cb = __ldg(a.conv_b + dd);
+    }
+    const float dsk = (a.Dskip && active) ? __ldg(a.Dskip + dd) : 0.0f;
+    const float bias = (a.delta_bias && active) ? __ldg(a.delta_bias + dd) : 0.0f;
+    const bool has_z = a.z != nullptr;
+
+    // adjoint of the final state, and the per-row gradient accumulators
+    float g[NS], da[NS];
+#pragma unroll
+    for (int n = 0; n < NS; ++n) {
+        g[n] = (a.dh_out && active && n < N) ? a.dh_out[row * N + n] : 0.0f;
+        da[n] = 0.0f;
+    }
+    float dD = 0.0f, dbias = 0.0f, dw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dcb = 0.0f;
+    float px[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // pending dx of x_t, x_{t-1}, x_{t-2}, x_{t-3}
+
+    // h_t of the step being processed; starts at h_{L-1}
+    const size_t hstride = (size_t)a.D * N;  // h_all: (B, L, D, N)
+    const float* hrow = a.h_all + ((size_t)b * L * a.D + dd) * N;
+    float hcur[NS];
+#pragma unroll
+    for (int n = 0; n < NS; ++n) hcur[n] = (active && n < N) ? hrow[(size_t)(L - 1) * hstride + n] : 0.0f;
+
+    const int last_chunk = ((L - 1) / kBwdChunk) * kBwdChunk;
+    for (int c0 = last_chunk; c0 >= 0; c0 -= kBwdChunk) {
+        const int clen = min(kBwdChunk, L - c0);
+        __syncthreads();  // everyone is done with the previous chunk's B / C
+        for (int i = tid; i < 2 * NS * kBwdChunk; i += kBwdThreads) {
+            const int wv = i / (NS * kBwdChunk);
+            const int rem = i - wv * NS * kBwdChunk;
+            const int n = rem / kBwdChunk, t = rem - n * kBwdChunk;
+            float val = 0.0f;
+            if (n < N && t < clen) val = load1<Tin>(wv ? a.Cm : a.Bm, ((size_t)b * N + n) * L + c0 + t);
+            sh.bc[wv][t][n] = val;
+        }
+        __syncthreads();
+        const int last_group = ((clen - 1) / kBwdGroup) * kBwdGroup;
+        for (int g0 = last_group; g0 >= 0; g0 -= kBwdGroup) {
+            const int tg = c0 + g0;
+            const int nv = min(kBwdGroup, clen - g0);
+            // inputs of the group's steps, and the conv inputs x_{tg-3} .. x_{tg-1} before them
+            float xv[kBwdGroup], dv[kBwdGroup], zv[kBwdGroup], gy[kBwdGroup], xh[3];
+            if (a.vec && nv == kBwdGroup && active) {  // 16-byte rows: vector loads
+                load8<Tin>(a.u, rowoff + tg, xv);
+                load8<Tin>(a.delta, rowoff + tg, dv);
+                if (has_z) load8<Tin>(a.z, rowoff + tg, zv);
+                load8<Tin>(a.dy, rowoff + tg, gy);
+                if (!has_z) {
+#pragma unroll
+                    for (int j = 0; j < kBwdGroup; ++j) zv[j] = 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kBwdGroup; ++j) {
+                    const bool ok = active && j < nv;
+                    xv[j] = ld<Tin>(a.u, rowoff + tg + j, ok);
+                    dv[j] = ld<Tin>(a.delta, rowoff + tg + j, ok);
+                    zv[j] = has_z ? ld<Tin>(a.z, rowoff + tg + j, ok) : 0.0f;
+                    gy[j] = ld<Tin>(a.dy, rowoff + tg + j, ok);
+                }
+            }
+            if (kConv) {
+                const int W1 = a.conv_width - 1;
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int t = tg - 3 + k;
+                    xh[k] = 0.0f;
+                    if (active && t >= 0) xh[k] = load1<Tin>(a.u, rowoff + t);
+                    else if (active && a.conv_init && t >= -W1) xh[k] = load1<Tin>(a.conv_init, row * W1 + W1 + t);
+                }
+            }
+            float du_o[kBwdGroup], dd_o[kBwdGroup], dz_o[kBwdGroup];
+#pragma unroll
+            for (int j = kBwdGroup - 1; j >= 0; --j) {
+                du_o[j] = dd_o[j] = dz_o[j] = 0.0f;
+                if (j >= nv) continue;  // uniform over the block: nv is
+                const int t = tg + j;
+                // recompute the step's scalars
+                float v, c = 0.0f, xm[4];
+                if (kConv) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int m = j - 3 + k;  // x_{t-3+k}
+                        xm[k] = m >= 0 ? xv[m >= 0 ? m : 0] : xh[m + 3 >= 0 ? m + 3 : 0];
+                    }
+                    c = fmaf(w[0], xm[0], cb);
+                    c = fmaf(w[1], xm[1], c);
+                    c = fmaf(w[2], xm[2], c);
+                    c = fmaf(w[3], xm[3], c);
+                    v = silu(c);
+                } else {
+                    v = xv[j];
+                }
+                const float s = dv[j] + bias;
+                const float dt = a.softplus ? softplus(s) : s;
+                // h_{t-1}: the previous step's state, or h0 before t = 0
+                float hprev[NS];
+                if (t > 0 && N == NS && active) {  // whole 16-byte rows of h_all
+                    const float4* hp4 = reinterpret_cast<const float4*>(hrow + (size_t)(t - 1) * hstride);
+#pragma unroll
+                    for (int k = 0; k < NS / 4; ++k) {
+                        const float4 q4 = __ldcs(hp4 + k);
+                        hprev[4 * k] = q4.x; hprev[4 * k + 1] = q4.y; hprev[4 * k + 2] = q4.z; hprev[4 * k + 3] = q4.w;
+                    }
+                } else if (t > 0) {
+#pragma unroll
+                    for (int n = 0; n < NS; ++n) hprev[n] = (active && n < N) ? hrow[(size_t)(t - 1) * hstride + n] : 0.0f;
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NS; ++n) hprev[n] = (a.h0 && active && n < N) ? a.h0[row * N + n] : 0.0f;
+                }
+                const float* Bt = sh.bc[0][t - c0];
+                const float* Ct = sh.bc[1][t - c0];
+                float yss = dsk * v;
+#pragma unroll
+                for (int n = 0; n < NS; ++n) yss = fmaf(Ct[n], hcur[n], yss);
+                float dyss = gy[j];
+                if (has_z) {
+                    const float sg = sigmoid_f(zv[j]);
+                    const float gz = zv[j] * sg;
+                    dz_o[j] = gy[j] * yss * sg * (1.0f + zv[j] * (1.0f - sg));
+                    dyss = gy[j] * gz;
+                }
+                dD = fmaf(dyss, v, dD);
+                float dvv = dsk * dyss, ddt = 0.0f;
+                float red[32];
+#pragma unroll
+                for (int n = 0; n < NS; ++n) {
+                    g[n] = fmaf(Ct[n], dyss, g[n]);
+                    red[16 + n] = dyss * hcur[n];                 // dC contribution
+                    const float x = dt * av[n];
+                    const float Ab = ex2(x * kLog2e);
+                    float E, dEdt, dEda;
+                    if (kZOH) {
+                        const bool nz = av[n] != 0.0f;
+                        E = nz ? (Ab - 1.0f) * inva[n] : dt;
+                        dEdt = Ab;
+                        dEda = nz ? (dt * Ab - E) * inva[n] : 0.5f * dt * dt;
+                    } else {
+                        E = dt;
+                        dEdt = 1.0f;
+                        dEda = 0.0f;
+                    }
+                    const float dAb = g[n] * hprev[n];
+                    const float dBb = g[n] * v;
+                    dvv = fmaf(g[n] * E, Bt[n], dvv);
+                    red[n] = dBb * E;                              // dB contribution
+                    const float dE = dBb * Bt[n];
+                    ddt = fmaf(dAb * Ab, av[n], fmaf(dE, dEdt, ddt));
+                    da[n] = fmaf(dAb * Ab, dt, fmaf(dE, dEda, da[n]));
+                    g[n] *= Ab;
+                }
+#pragma unroll
+                for (int n = NS; n < 16; ++n) red[n] = red[16 + n] = 0.0f;
+                const float ds = a.softplus ? ddt * sigmoid_f(s) : ddt;
+                dbias += ds;
+                dd_o[j] = ds;
+                if (kConv) {
+                    const float sc = sigmoid_f(c);
+                    const float dc = dvv * sc * (1.0f + c * (1.0f - sc));
+                    dcb += dc;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        dw[k] = fmaf(dc, xm[k], dw[k]);
+                        px[3 - k] = fmaf(dc, w[k], px[3 - k]);     // x_{t-3+k} is pending slot 3 - k
+                    }
+                    du_o[j] = px[0];
+                    px[0] = px[1];
+                    px[1] = px[2];
+                    px[2] = px[3];
+                    px[3] = 0.0f;
+                } else {
+                    du_o[j] = dvv;
+                }
+#pragma unroll
+                for (int n = 0; n < NS; ++n) hcur[n] = hprev[n];
+                // the warp's sum of each of the 32 values: transpose through shared memory
+                if (!active) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) red[k] = 0.0f;
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) sh.tr[warp][k][lane] = red[k];
+                __syncwarp();
+                float sum = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) sum += sh.tr[warp][lane][k];
+                sh.ws[warp][j][lane] = sum;
+                __syncwarp();
+            }
+            // outputs of the group
+            if (active && a.vec && nv == kBwdGroup) {
+                store8<Tin>(a.du, rowoff + tg, du_o);
+                store8<Tin>(a.ddelta, rowoff + tg, dd_o);
+                if (has_z) store8<Tin>(a.dz, rowoff + tg, dz_o);
+            } else if (active) {
+#pragma unroll
+                for (int j = 0; j < kBwdGroup; ++j) {
+                    if (j < nv) {
+                        store1<Tin>(a.du, rowoff + tg + j, du_o[j]);
+                        store1<Tin>(a.ddelta, rowoff + tg + j, dd_o[j]);
+                        if (has_z) store1<Tin>(a.dz, rowoff + tg + j, dz_o[j]);
+                    }
+                }
+            }
+            // dB, dC of the group: the four warps' sums, one atomic per (n, t)
+            __syncthreads();
+            for (int i = tid; i < kBwdGroup * 32; i += kBwdThreads) {
+                const int j = i >> 5, k = i & 31;
+                const int n = k & 15;
+                if (j < nv && n < N) {
+                    float tot = 0.0f;
+#pragma unroll
+                    for (int wv = 0; wv < kBwdThreads / 32; ++wv) tot += sh.ws[wv][j][k];
+                    float* dst = (k < 16 ? a.dB : a.dC) + ((size_t)b * N + n) * L + tg + j;
+                    atomicAdd(dst, tot);
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    if (!active) return;
+    // the adjoint before t = 0, and the conv history's gradient
+    if (a.dh0) {
+#pragma unroll
+        for (int n = 0; n < NS; ++n)
+            if (n < N) a.dh0[row * N + n] = g[n];
+    }
+    if (kConv && a.dconv_init) {
+        const int W1 = a.conv_width - 1;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)  // px[k] holds dx of x_{-1-k}
+            if (k < W1) store1<Tin>(a.dconv_init, row * W1 + W1 - 1 - k, px[k]);
+    }
+#pragma unroll
+    for (int n = 0; n < NS; ++n)
+        if (n < N) atomicAdd(a.dA + (size_t)dd * N + n, da[n]);
+    if (a.dDskip) atomicAdd(a.dDskip + dd, dD);
+    if (a.ddelta_bias) atomicAdd(a.ddelta_bias + dd, dbias);
+    if (kConv) {
+        const int W = a.conv_width;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i >= 4 - W && a.dconv_w) atomicAdd(a.dconv_w + (size_t)dd * W + i - (4 - W), dw[i]);
+        if (a.dconv_b) atomicAdd(a.dconv_b + dd, dcb);
+    }
+}
+
+template <typename Tin, int NS, bool kZOH>
+cudaError_t launch_bwd_z(const ScanBwdArgs& a, cudaStream_t s) {
+    dim3 grid((unsigned)((a.D + kBwdThreads - 1) / kBwdThreads), (unsigned)a.Bsz);
+    if (a.conv_w) scan_bwd_kernel<Tin, NS, kZOH, true><<<grid, kBwdThreads, 0, s>>>(a);
+    else scan_bwd_kernel<Tin, NS, kZOH, false><<<grid, kBwdThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int NS>
+cudaError_t launch_bwd_n(const ScanBwdArgs& a, int zoh, cudaStream_t s) {
+    return zoh ? launch_bwd_z<Tin, NS, true>(a, s) : launch_bwd_z<Tin, NS, false>(a, s);
+}
+
+template <typename Tin>
+cudaError_t launch_bwd_t(const ScanBwdArgs& a, int zoh, cudaStream_t s) {
+    if (a.N <= 4) return launch_bwd_n<Tin, 4>(a, zoh, s);
+    if (a.N <= 8) return launch_bwd_n<Tin, 8>(a, zoh, s);
+    return launch_bwd_n<Tin, 16>(a, zoh, s);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream) {
+    return dtype == 1 ? launch_bwd_t<BF16>(a, zoh, stream) : launch_bwd_t<F32>(a, zoh, stream);
+}
+
+}  // namespace ssm

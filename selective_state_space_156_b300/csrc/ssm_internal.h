@@ -87,6 +87,43 @@ bool state_update_bulk_eligible(const DecodeStep& s);
 cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream);
 cudaError_t take_bulk_wait_error(unsigned* flags);
 
+// The backward pass (scan_bwd.cu), after host-side validation and zeroing of the accumulated outputs.
+struct ScanBwdArgs {
+    int Bsz, D, N, L;
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* Bm;
+    const void* Cm;
+    const float* Dskip;
+    const float* delta_bias;
+    const void* z;
+    const float* conv_w;
+    const float* conv_b;
+    int conv_width;
+    const void* conv_init;
+    const float* h0;
+    const float* h_all;   // (B, L, D, N) the forward's state after every step
+    const void* dy;
+    const float* dh_out;  // (B, D, N) or NULL
+    void* du;
+    void* ddelta;
+    void* dz;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dDskip;
+    float* ddelta_bias;
+    float* dconv_w;
+    float* dconv_b;
+    void* dconv_init;
+    float* dh0;
+    int softplus;
+    int vec;  // every (b, d) row of u / delta / z / dy / du / ddelta / dz is 16-byte aligned and L % 8 == 0
+};
+
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream);
+
 // Launch geometry of each kernel kind, used by the host to plan the L split.
 constexpr int kSeqChanPerBlock = 128, kSeqBlocksPerSM = 3, kSeqChunk = 64;
 constexpr int kG4ChanPerBlock = 32, kG4BlocksPerSM = 7, kG4ChunkSteps = 32;

@@ -199,3 +199,35 @@ def test_scan_rejects_conv_final_overlapping_an_input(L):
     p = _params(conv_w=(1 << 40) + (7 << 30), conv_width=4, conv_final=(1 << 40) + 64)  # inside u
     assert L.ssm_scan_fwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
     assert "conv_final overlaps" in L.ssm_last_error().decode()
+
+
+def test_bwd_params_struct_layout_matches_c():
+    got = _c_layout("ssm_scan_bwd_params", """
+  F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip) F(delta_bias) F(z)
+  F(conv_w) F(conv_b) F(conv_width) F(conv_init) F(h0) F(delta_softplus) F(zoh) F(h_all) F(dy) F(dh_out) F(du)
+  F(ddelta) F(dz) F(dA) F(dB) F(dC) F(dDskip) F(ddelta_bias) F(dconv_w) F(dconv_b) F(dconv_init) F(dh0)""")
+    assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanBwdParams)
+    assert len(got) == len(ssm.ScanBwdParams._fields_)
+    for name, off in got.items():
+        assert getattr(ssm.ScanBwdParams, name).offset == int(off), name
+
+
+def test_bwd_rejects_bad_arguments_on_host(L):
+    p = ssm.ScanBwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.in_dtype = 2, 64, 16, 128, ssm.SSM_BF16
+    fake = 1 << 40
+    for i, k in enumerate(["u", "delta", "A", "Bm", "Cm", "h_all", "dy", "du", "ddelta", "dA", "dB", "dC"]):
+        setattr(p, k, fake + (i << 32))
+    p.delta_softplus, p.zoh = 1, 1
+    p.dstate = 32
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_UNSUPPORTED
+    p.dstate = 16
+    p.dy = None
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    p.dy = fake + (6 << 32)
+    p.z = fake + (20 << 32)  # z without dz
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    p.z = None
+    p.du = p.u + 128  # an output inside an input
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "overlaps" in L.ssm_last_error().decode()
