@@ -287,6 +287,14 @@ def run_b300(args, rank, world, local):
     import selective_state_space_156_b300 as ssm
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.backward_only:  # the training step alone (profiling runs)
+        cfg = workloads.SCAN_CONFIGS[args.workload]
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in rank_inputs(cfg, rank).items()}
+        hbm_peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+        out = run_backward(ssm, dev, cfg, g, hbm_peak, world, steps=max(args.steps, 1))
+        if rank == 0:
+            print(json.dumps({"backward": out}), flush=True)
+        return
     if args.decode_only:  # the decode workload alone (profiling runs; smaller with --decode-layers/steps)
         hbm_peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
         decode = run_decode(ssm, dev, hbm_peak, world, steps=args.decode_steps, nlayers=args.decode_layers)
@@ -406,6 +414,11 @@ def run_b300(args, rank, world, local):
     hbm = {"achieved_gbs": nbytes / t_s / 1e9, "peak_gbs": hbm_peak, "frac": nbytes / t_s / 1e9 / hbm_peak,
            "bytes_per_launch": nbytes, "peak_source": hbm_src}
 
+    # --- a training step: forward keeping every state, then the backward pass ---
+    backward = None
+    if not args.no_backward:
+        backward = run_backward(ssm, dev, cfg, g, hbm_peak, world)
+
     # --- decode workload (ssm_state_update) ---
     decode = None
     if not args.no_decode:
@@ -426,7 +439,7 @@ def run_b300(args, rank, world, local):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(cfg, world),
             "gpu_launches": K * launches_per_step,
-            "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+            "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode, "backward": backward,
             "clocks": clk.summary(), "wall_s_timed_region": wall, "mufu_probe": probe,
             "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
         }
@@ -483,6 +496,53 @@ def run_decode(ssm, dev, hbm_peak, world, steps=None, nlayers=None):
             "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_call": per_call, "launch": "CUDA graph per token"}
 
 
+def run_backward(ssm, dev, cfg, g, hbm_peak, world, steps=5):
+    """A training step of the layer: the forward that keeps the state after every step (h_all, (B, L, D, N)
+    fp32), then ssm_scan_bwd over it.  Reported beside the forward-only headline, with the HBM bytes each
+    launch must move at least."""
+    Bsz, D, L = g["u"].shape
+    N = g["A"].shape[1]
+    h_all = torch.empty((Bsz, L, D, N), dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(17)
+    dy = torch.randn((Bsz, D, L), generator=gen, device=dev).to(g["u"].dtype)
+    kw = dict(Dskip=g["Dskip"], delta_bias=g["delta_bias"], z=g["z"], conv_w=g["conv_w"], conv_b=g["conv_b"])
+    y = torch.empty_like(g["u"])
+
+    def fwd():
+        ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], y=y, h_all=h_all, **kw)
+
+    def bwd():
+        return ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dy, h_all, **kw)
+
+    for _ in range(2):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record()
+        fwd()
+        ev[i][1].record()
+        bwd()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    t_f = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    t_b = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    t_f, t_b = max_over_ranks(t_f, world), max_over_ranks(t_b, world)
+    e = g["u"].element_size()
+    bdl = Bsz * D * L
+    hall_bytes = bdl * N * 4
+    fwd_bytes = bdl * e * 4 + hall_bytes                        # u, delta, z in; y out; every state out
+    bwd_bytes = bdl * e * 7 + hall_bytes + 2 * Bsz * N * L * 4  # u, delta, z, dy in; du, ddelta, dz out; states
+    return {"workload": f"{cfg.name}: forward keeping every state (h_all) + ssm_scan_bwd",
+            "ms_forward_h_all": t_f, "ms_backward": t_b,
+            "elements_per_s_train_step": world * bdl * N / ((t_f + t_b) * 1e-3),
+            "forward_hbm_gbs": fwd_bytes / (t_f * 1e-3) / 1e9, "forward_hbm_frac": fwd_bytes / (t_f * 1e-3) / 1e9 / hbm_peak,
+            "backward_hbm_gbs": bwd_bytes / (t_b * 1e-3) / 1e9,
+            "backward_hbm_frac": bwd_bytes / (t_b * 1e-3) / 1e9 / hbm_peak,
+            "bytes_forward": fwd_bytes, "bytes_backward": bwd_bytes, "steps": steps}
+
+
 # ---------------------------------------------------------------------------------------------
 # the reference arm: the oracle as it stands, on the host cores
 # ---------------------------------------------------------------------------------------------
@@ -531,6 +591,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of this kernel (reported as is)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the training-step (backward) measurement")
+    ap.add_argument("--backward-only", action="store_true", help="run only the training-step measurement")
     ap.add_argument("--decode-only", action="store_true", help="run only the decode workload")
     ap.add_argument("--decode-layers", type=int, default=None, help="decode layers (default 64)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode tokens (default 128)")

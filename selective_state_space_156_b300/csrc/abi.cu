@@ -56,11 +56,12 @@ bool aligned_rows(const ssm_scan_params* p) {
 }
 
 int scan_kind(const ssm_scan_params* p) {
-    // state slots and the per-step state output are implemented by the element-wise kernel
-    if (p->state_indices != nullptr || p->h_all != nullptr) return ssm::kScanSeq;
+    // state slots are implemented by the element-wise kernel; the per-step state output by it and by the
+    // packed kernel (16-byte-aligned h_all)
+    if (p->state_indices != nullptr) return ssm::kScanSeq;
     if (p->in_dtype == SSM_BF16 && p->out_dtype == SSM_BF16 && aligned_rows(p)) {
-        if (p->dstate <= 16) return ssm::kScanP16;
-        if (p->dstate <= 64) return ssm::kScanG4;
+        if (p->dstate <= 16 && (p->h_all == nullptr || aligned16(p->h_all))) return ssm::kScanP16;
+        if (p->dstate <= 64 && p->h_all == nullptr) return ssm::kScanG4;
     }
     return ssm::kScanSeq;
 }

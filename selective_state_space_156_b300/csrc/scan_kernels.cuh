@@ -132,9 +132,15 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
         if (kFinal && hall != nullptr) {
             // the state after step tg + j: row (b, tg + j, d) of h_all, stride D * N per step
             float* hp = hall + (size_t)(tg + j) * a.D * a.N;
+            if (a.N == NS && (reinterpret_cast<uintptr_t>(a.h_all) & 15) == 0) {  // whole rows: 16-byte stores
 #pragma unroll
-            for (int n = 0; n < NS; ++n)
-                if (n < a.N) hp[n] = h[n];
+                for (int n = 0; n < NS; n += 4)
+                    *reinterpret_cast<float4*>(hp + n) = make_float4(h[n], h[n + 1], h[n + 2], h[n + 3]);
+            } else {
+#pragma unroll
+                for (int n = 0; n < NS; ++n)
+                    if (n < a.N) hp[n] = h[n];
+            }
         }
     }
 

@@ -102,11 +102,11 @@ struct P16Consts {
 };
 
 // 8 steps starting at chunk column j0 (all inside [t_begin, t_end)).
-template <int NS, int LPC, Disc kDisc, bool kFinal, bool kConv>
+template <int NS, int LPC, Disc kDisc, bool kFinal, bool kConv, bool kHall>
 __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem<NS, LPC>& sm, int buf, int j0,
                                           const P16Consts<NS / LPC>& cc, const float (&w)[4], float cb, float dskip,
                                           float bias, f32x2 (&hp)[NS / LPC / 2], float& dsum, bool has_z,
-                                          bool active, size_t yoff) {
+                                          bool active, size_t yoff, float* hall) {
     constexpr int NSL = NS / LPC;   // states per lane
     constexpr int SPL = 8 / LPC;    // steps whose scalars this lane owns
     const int lane = threadIdx.x & 31;
@@ -213,6 +213,23 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
                 acc = fma2(cq.y, hp[p4 + 1], acc);
             }
         }
+        if (kHall && active) {
+            // the state after this step, into h_all (B, L, D, N): this lane's states, 16-byte stores
+            float* hp_out = hall + (size_t)(j0 + j) * a.D * a.N;
+            if (a.N == NS) {
+#pragma unroll
+                for (int p = 0; p < NSL / 2; p += 2)
+                    *reinterpret_cast<ulonglong2*>(hp_out + 2 * p) = make_ulonglong2(hp[p], hp[p + 1]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < NSL / 2; ++p) {
+                    float h0_, h1_;
+                    unpack2(hp[p], h0_, h1_);
+                    if (e * NSL + 2 * p < a.N) hp_out[2 * p] = h0_;
+                    if (e * NSL + 2 * p + 1 < a.N) hp_out[2 * p + 1] = h1_;
+                }
+            }
+        }
         if (kFinal) {
             float ya, yb;
             unpack2(acc, ya, yb);
@@ -241,7 +258,7 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 // Resident blocks per SM the register budget aims at, by lanes per channel.
 __host__ __device__ constexpr int p16_min_blocks(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
 
-template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv>
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false>
 __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_kernel(const ScanKernelArgs a) {
     constexpr int NSL = NS / LPC;
     constexpr int kCh = P16Smem<NS, LPC>::kCh;
@@ -357,13 +374,15 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
         const int clen = min(kP16Chunk, t_end - c0);
         // every lane of a warp takes part (the shuffles need them); inactive channels write nothing
         for (int j0 = 0; j0 < clen; j0 += 8) {
+            float* hall = kHall ? a.h_all + ((size_t)b * a.L * a.D + (active ? d : 0)) * a.N + e * NSL +
+                                          (size_t)c0 * a.D * a.N
+                                : nullptr;
             if (safe)
-                p16_group<NS, LPC, Disc::kZOHSafe, kFinal, kConv>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum, has_z,
-                                                                   active, yoff + c0);
+                p16_group<NS, LPC, Disc::kZOHSafe, kFinal, kConv, kHall>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum,
+                                                                          has_z, active, yoff + c0, hall);
             else
-                p16_group<NS, LPC, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv>(a, sm, buf, j0, cc, w, cb, dskip,
-                                                                                   bias, hp, dsum, has_z, active,
-                                                                                   yoff + c0);
+                p16_group<NS, LPC, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv, kHall>(
+                    a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum, has_z, active, yoff + c0, hall);
         }
     }
 
@@ -399,7 +418,8 @@ cudaError_t launch_p16_ns(const ScanKernelArgs& a, cudaStream_t stream) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    auto kfn = scan_p16_kernel<NS, LPC, kZOH, true, kConv>;
+    auto kfn = a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true>
+                                  : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false>;
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a);

@@ -29,9 +29,12 @@ def _kw(g):
 
 
 @pytest.mark.parametrize("dt,N,D,L", [("bf16", 16, 64, 4), ("bf16", 16, 150, 1), ("f32", 4, 64, 13),
-                                      ("bf16", 8, 128, 8), ("f32", 16, 32, 3000)])
+                                      ("bf16", 8, 128, 8), ("f32", 16, 32, 3000), ("bf16", 16, 256, 64),
+                                      ("bf16", 12, 128, 40), ("bf16", 16, 64, 2048)])
 def test_multi_token_pass_returns_every_state(dt, N, D, L):
-    """y, the final state and the state after every step; (f32, 16, 32, 3000) takes the L split."""
+    """y, the final state and the state after every step.  bf16 with L % 8 == 0 takes the packed kernel
+    ((16, 64, 2048) with the L split, N = 12 with padded states); the rest the element-wise kernel,
+    (f32, 16, 32, 3000) with the L split."""
     Bsz = 3
     d = _inputs(Bsz, D, N, L, dt, seed=7000 + N + D + L)
     g = to_dev(d)
