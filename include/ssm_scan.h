@@ -251,11 +251,13 @@ SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t strea
 
 /*
  * Device-side failures that a kernel could only record, not return.  (No counterpart on the pages.)
- * The streamed decode kernel bounds every wait for its own bulk copies to about one second; on a
- * timeout it sets a bit in a per-device flag, lets its copies still in flight land (again bounded) and
- * returns, leaving the outputs of the affected tiles unwritten and the context usable.  This call
- * synchronises the current device, stores the flag in *flags (0: nothing recorded; bit 0: a decode
- * wait timed out) and clears it.
+ * The streamed decode kernel and the packed scan kernel bound every wait for their own bulk copies to
+ * about one second; on a timeout they set a bit in a per-device flag, let their copies still in flight
+ * land (again bounded) and return, leaving the outputs of the affected tiles unwritten and the context
+ * usable.  This call
+ * synchronises the current device, stores the flags in *flags (0: nothing recorded; bit 0: a decode
+ * wait timed out; bit 1: a scan block stopped waiting for its staged chunk, likewise bounded) and
+ * clears them.
  * Errors: SSM_ERR_INVALID_ARG (flags NULL), SSM_ERR_CUDA (the synchronisation or the read failed).
  */
 SSM_API ssm_status ssm_device_error(unsigned *flags);

@@ -349,7 +349,8 @@ def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, 
 
 def ssm_device_error() -> int:
     """Synchronises the current device and returns (and clears) the flags that kernels record when a
-    bounded wait runs out: 0 when nothing was recorded, bit 0 for a decode-kernel wait."""
+    bounded wait runs out: 0 when nothing was recorded, bit 0 for a decode-kernel wait, bit 1 for a scan
+    kernel's wait for its staged chunk."""
     flags = ctypes.c_uint(0)
     _check(lib().ssm_device_error(ctypes.byref(flags)))
     return int(flags.value)

@@ -348,7 +348,13 @@ ssm_status ssm_device_error(unsigned* flags) {
     if (flags == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_device_error: flags is NULL");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: cudaDeviceSynchronize");
-    return cuda_status(ssm::take_bulk_wait_error(flags), "ssm_device_error: reading the flag");
+    unsigned dec = 0, scan = 0;
+    e = ssm::take_bulk_wait_error(&dec);
+    if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: reading the decode flag");
+    e = ssm::take_scan_wait_error(&scan);
+    if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: reading the scan flag");
+    *flags = (dec ? 1u : 0u) | (scan ? 2u : 0u);
+    return SSM_OK;
 }
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {

@@ -20,4 +20,11 @@ cudaError_t launch_scan_bf16_bf16(const ScanKernelArgs& a, int zoh, cudaStream_t
     }
     return launch_scan_typed<BF16, BF16>(a, zoh, s);
 }
+
+cudaError_t take_scan_wait_error(unsigned* flags) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_scan_wait_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_scan_wait_error, &zero, sizeof(unsigned));
+}
 }  // namespace ssm

@@ -25,8 +25,12 @@
 // 16-byte-aligned rows (the host checks).  bf16 outputs use MUFU tanh/lg2 forms of SiLU and softplus.
 #pragma once
 
+#include <cstdlib>
+#include <cstring>
+
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
+#include "tma.cuh"
 
 namespace ssm {
 
@@ -39,17 +43,48 @@ constexpr int kP16Segs = kP16Chunk / 8;       // 16-byte segments per staged row
 template <int NS, int LPC>
 struct P16Smem {
     static constexpr int kCh = kP16Threads / LPC;  // channels per block
+    static constexpr int kNSR = NS < 8 ? 8 : NS;   // B / C rows per block of bcr: a multiple of 128 bytes
+    // every tile that a bulk tensor copy fills starts on a 128-byte boundary (rows of 80 bytes: 8 rows
+    // = 640 bytes, and kCh, kNSR are multiples of 8)
     uint16_t x[2][kCh][kP16Row];               // bf16 u / x, steps c0-8 .. c0+31
     uint16_t dl[2][kCh][kP16Row];              // bf16 delta at [8 + t - c0]
     uint16_t zz[2][kCh][kP16Row];              // bf16 z at [8 + t - c0]
-    uint16_t bcr[2][2][NS][kP16Row];           // raw bf16 B / C rows (n, t), padded against bank conflicts
+    uint16_t bcr[2][2][kNSR][kP16Row];         // raw bf16 B / C rows (n, t), padded against bank conflicts
     float bc[kP16Chunk][2][NS];                // fp32 B_t[n], C_t[n]
+    uint64_t bar[2];                           // mbarriers of the two chunk buffers (bulk-copy staging)
 };
 
 __device__ __forceinline__ void p16_cp_async16(void* smem, const void* gmem, bool valid) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     const int n = valid ? 16 : 0;  // 0: fill the 16 bytes with zeros, read nothing
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+
+// Tensor maps of the tiled bulk copies (TMA) that stage a chunk: x (with the conv halo), delta, z as
+// (L, B*D) matrices with boxes of 40 steps x the block's channels, B and C as (L, B*N) matrices with
+// boxes of 40 steps x NS states.  Every box starts 8 steps before the chunk, so the staged rows have
+// the layout of the per-thread copies below (the chunk at column 8); rows past the matrix come in as
+// zeros, and B / C rows of the next batch row (n >= N) are masked when they are widened.
+struct P16Maps {
+    CUtensorMap x, dl, zz, B, C;
+};
+
+// Set when a wait for a chunk's copies ran out (about a second): the block then leaves its outputs
+// unwritten.  Read and cleared by take_scan_wait_error (ssm_device_error).
+static __device__ unsigned int g_scan_wait_error = 0;
+
+template <int NS, int LPC>
+__device__ __forceinline__ void p16_tma_chunk(const P16Maps& maps, P16Smem<NS, LPC>& sm, uint64_t* bar, int buf,
+                                              int row0, int brow0, int c0, bool want_z) {
+    constexpr int kCh = P16Smem<NS, LPC>::kCh;
+    constexpr unsigned kRowBytes = kP16Row * 2;
+    const unsigned bytes = kRowBytes * (2u * kCh + (want_z ? kCh : 0u) + 2u * NS);
+    mbar_arrive_expect_tx(bar, bytes);
+    tma_load_2d(&sm.x[buf][0][0], &maps.x, c0 - kP16Halo, row0, bar);
+    tma_load_2d(&sm.dl[buf][0][0], &maps.dl, c0 - kP16Halo, row0, bar);
+    if (want_z) tma_load_2d(&sm.zz[buf][0][0], &maps.zz, c0 - kP16Halo, row0, bar);
+    tma_load_2d(&sm.bcr[buf][0][0][0], &maps.B, c0 - kP16Halo, brow0, bar);
+    tma_load_2d(&sm.bcr[buf][1][0][0], &maps.C, c0 - kP16Halo, brow0, bar);
 }
 
 template <int NS, int LPC>
@@ -258,12 +293,15 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 // Resident blocks per SM the register budget aims at, by lanes per channel.
 __host__ __device__ constexpr int p16_min_blocks(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
 
-template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false>
-__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_kernel(const ScanKernelArgs a) {
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false, bool kTma = false>
+__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
+    scan_p16_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
     constexpr int NSL = NS / LPC;
     constexpr int kCh = P16Smem<NS, LPC>::kCh;
-    extern __shared__ __align__(16) unsigned char p16_smem_raw[];
+    constexpr int kBcOff = kTma ? kP16Halo : 0;  // column of the chunk's first step in the staged B / C rows
+    extern __shared__ __align__(128) unsigned char p16_smem_raw[];
     P16Smem<NS, LPC>& sm = *reinterpret_cast<P16Smem<NS, LPC>*>(p16_smem_raw);
+    uint64_t* tma_bar = sm.bar;
     const int tid = threadIdx.x;
     const int e = tid & (LPC - 1);
     const int b = blockIdx.y, seg = blockIdx.z;
@@ -277,9 +315,24 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
     const bool has_z = kFinal && a.z != nullptr;
 
     // B/C rows past N stay zero (cp.async never writes them)
-    for (int i = tid; i < 2 * 2 * NS * kP16Row; i += kP16Threads) (&sm.bcr[0][0][0][0])[i] = 0;
+    for (int i = tid; i < 2 * 2 * P16Smem<NS, LPC>::kNSR * kP16Row; i += kP16Threads) (&sm.bcr[0][0][0][0])[i] = 0;
+    const int row0 = b * a.D + ch0, brow0 = b * a.N;
+    if (kTma && tid == 0) {
+        tma_prefetch_map(&maps.x);
+        tma_prefetch_map(&maps.dl);
+        if (has_z) tma_prefetch_map(&maps.zz);
+        tma_prefetch_map(&maps.B);
+        tma_prefetch_map(&maps.C);
+        mbar_init(&tma_bar[0], 1);
+        mbar_init(&tma_bar[1], 1);
+        mbar_fence_init();
+    }
     __syncthreads();
-    p16_issue_chunk<NS, LPC>(a, sm, 0, b, ch0, t_begin, has_z);
+    if (kTma) {
+        if (tid == 0) p16_tma_chunk<NS, LPC>(maps, sm, &tma_bar[0], 0, row0, brow0, t_begin, has_z);
+    } else {
+        p16_issue_chunk<NS, LPC>(a, sm, 0, b, ch0, t_begin, has_z);
+    }
 
     P16Consts<NSL> cc;
     bool has_zero = false;
@@ -348,11 +401,26 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
     const bool safe = kZOH && __syncthreads_or(has_zero);  // block-uniform choice of loop body
     const size_t yoff = row * (size_t)a.L;
 
-    int buf = 0;
-    for (int c0 = t_begin; c0 < t_end; c0 += kP16Chunk, buf ^= 1) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();  // chunk c0 landed for every thread; everyone is done with the other buffers
-        if (c0 + kP16Chunk < t_end) p16_issue_chunk<NS, LPC>(a, sm, buf ^ 1, b, ch0, c0 + kP16Chunk, has_z);
+    int buf = 0, k = 0;
+    for (int c0 = t_begin; c0 < t_end; c0 += kP16Chunk, buf ^= 1, ++k) {
+        if (kTma) {
+            // the chunk's copies have landed (bounded wait; a block that gives up writes nothing more)
+            const bool ok = mbar_wait_bounded(&tma_bar[buf], (unsigned)((k >> 1) & 1));
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    atomicOr(&g_scan_wait_error, 1u);
+                    mbar_wait_bounded(&tma_bar[buf], (unsigned)((k >> 1) & 1));
+                }
+                return;
+            }
+            // every thread is done with the other buffers: refill them with the next chunk
+            if (tid == 0 && c0 + kP16Chunk < t_end)
+                p16_tma_chunk<NS, LPC>(maps, sm, &tma_bar[buf ^ 1], buf ^ 1, row0, brow0, c0 + kP16Chunk, has_z);
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            __syncthreads();  // chunk c0 landed for every thread; everyone is done with the other buffers
+            if (c0 + kP16Chunk < t_end) p16_issue_chunk<NS, LPC>(a, sm, buf ^ 1, b, ch0, c0 + kP16Chunk, has_z);
+        }
         if (kConv && c0 == 0 && a.conv_init != nullptr) {
             // x before t = 0 is the caller's history (oldest first), not the zeros the copy filled in
             const int W1 = a.conv_width - 1;
@@ -368,7 +436,7 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
             const int t = i / (2 * NS);
             const int rem = i - t * 2 * NS;
             const int wv = rem / NS, n = rem - wv * NS;
-            sm.bc[t][wv][n] = bf16_to_f32(sm.bcr[buf][wv][n][t]);
+            sm.bc[t][wv][n] = n < a.N ? bf16_to_f32(sm.bcr[buf][wv][n][kBcOff + t]) : 0.0f;
         }
         __syncthreads();
         const int clen = min(kP16Chunk, t_end - c0);
@@ -403,27 +471,58 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC)) scan_p16_ker
     }
 }
 
-template <int NS, int LPC, bool kZOH, bool kConv>
-cudaError_t launch_p16_ns(const ScanKernelArgs& a, cudaStream_t stream) {
+// SSM_SCAN_STAGING=cpasync stages chunks with per-thread cp.async copies instead of the tiled bulk copies
+// (for comparisons); the bulk copies are also skipped when a tensor map cannot be encoded.
+inline bool p16_use_tma() {
+    static const bool on = [] {
+        const char* v = std::getenv("SSM_SCAN_STAGING");
+        return !(v != nullptr && std::strcmp(v, "cpasync") == 0);
+    }();
+    return on;
+}
+
+template <int NS, int LPC>
+inline bool p16_encode_maps(const ScanKernelArgs& a, P16Maps& m) {
+    constexpr int kCh = P16Smem<NS, LPC>::kCh;
+    const uint64_t L = (uint64_t)a.L, rows = (uint64_t)a.Bsz * a.D, brows = (uint64_t)a.Bsz * a.N;
+    bool ok = encode_bf16_map_2d(&m.x, a.u, L, rows, L * 2, kP16Row, kCh) &&
+              encode_bf16_map_2d(&m.dl, a.delta, L, rows, L * 2, kP16Row, kCh) &&
+              encode_bf16_map_2d(&m.B, a.Bm, L, brows, L * 2, kP16Row, NS) &&
+              encode_bf16_map_2d(&m.C, a.Cm, L, brows, L * 2, kP16Row, NS);
+    if (ok && a.z != nullptr) ok = encode_bf16_map_2d(&m.zz, a.z, L, rows, L * 2, kP16Row, kCh);
+    if (ok && a.z == nullptr) m.zz = m.x;  // never read: the z copy is skipped
+    return ok;
+}
+
+template <int NS, int LPC, bool kZOH, bool kConv, bool kTma>
+cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cudaStream_t stream) {
     const size_t smem = sizeof(P16Smem<NS, LPC>);
     constexpr int kCh = P16Smem<NS, LPC>::kCh;
     dim3 block(kP16Threads);
     const unsigned gx = (unsigned)((a.D + kCh - 1) / kCh);
     cudaError_t e;
     if (a.nseg > 1) {
-        auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv>;
+        auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv, false, kTma>;
         e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a);
+        kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a, maps);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    auto kfn = a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true>
-                                  : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false>;
+    auto kfn = a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true, kTma>
+                                  : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma>;
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a);
+    kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a, maps);
     return cudaGetLastError();
+}
+
+template <int NS, int LPC, bool kZOH, bool kConv>
+cudaError_t launch_p16_ns(const ScanKernelArgs& a, cudaStream_t stream) {
+    P16Maps maps{};
+    if (p16_use_tma() && p16_encode_maps<NS, LPC>(a, maps))
+        return launch_p16_staged<NS, LPC, kZOH, kConv, true>(a, maps, stream);
+    return launch_p16_staged<NS, LPC, kZOH, kConv, false>(a, maps, stream);
 }
 
 template <int NS, int LPC>

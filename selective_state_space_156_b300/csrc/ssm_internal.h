@@ -86,6 +86,8 @@ cudaError_t launch_state_update(const DecodeStep& s, cudaStream_t stream);
 bool state_update_bulk_eligible(const DecodeStep& s);
 cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream);
 cudaError_t take_bulk_wait_error(unsigned* flags);
+// The packed scan kernel's flag for a chunk whose bulk tensor copies it stopped waiting for.
+cudaError_t take_scan_wait_error(unsigned* flags);
 
 // The backward pass (scan_bwd.cu), after host-side validation and zeroing of the accumulated outputs.
 struct ScanBwdArgs {

@@ -1,0 +1,44 @@
+// Host side of the tiled bulk-tensor copies: the driver's tensor-map encoder, looked up once through the
+// runtime so that the library does not link against libcuda.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "tma.cuh"
+
+namespace ssm {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool encode_bf16_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
+                        uint32_t box_inner, uint32_t box_rows) {
+    auto fn = encoder();
+    if (fn == nullptr) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || stride_bytes % 16 != 0 || (box_inner * 2) % 16 != 0)
+        return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace ssm
