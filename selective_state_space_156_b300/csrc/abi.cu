@@ -71,7 +71,7 @@ struct KindGeom {
 };
 
 // Resident blocks per SM of the packed kernel by lanes per channel (its launch bounds).
-int p16_blocks_per_sm(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
+int p16_blocks_per_sm(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 6); }  // registers, or shared memory (lpc 4)
 
 KindGeom kind_geom(int kind, int lpc) {
     if (kind == ssm::kScanG4) return {ssm::kG4ChanPerBlock, ssm::kG4BlocksPerSM, ssm::kG4ChunkSteps};

@@ -18,10 +18,11 @@
 // whose fixed point for a constant input is -ng exactly, whatever the rounding of Abar.  A block in
 // which some a == 0 runs a second loop body that uses the a -> 0 limit dt B (lshu.cn/news/79586 2.2).
 //
-// Staging.  Per 32-step chunk, cp.async copies the block's u/x rows (with an 8-step halo for the conv
-// front end of dpshk.com/news/3333417 section 5.2), delta and z rows and the B/C rows of the batch row
-// into shared memory one chunk ahead (double buffer); B/C are widened to fp32 once per chunk and read
-// by every lane as broadcasts.  Outputs leave as 16-byte stores of 8 steps.  Requires L % 8 == 0 and
+// Staging.  Per 48-step chunk, five tiled bulk tensor copies (TMA, issued by one thread, completing on
+// an mbarrier) bring the block's u/x rows (with an 8-step halo for the conv front end of
+// dpshk.com/news/3333417 section 5.2), delta and z rows and the B/C rows of the batch row into shared
+// memory one chunk ahead (double buffer); per-thread cp.async copies remain as the alternative.  B/C
+// are widened to fp32 once per chunk and read by every lane as broadcasts.  Outputs leave as 16-byte stores of 8 steps.  Requires L % 8 == 0 and
 // 16-byte-aligned rows (the host checks).  bf16 outputs use MUFU tanh/lg2 forms of SiLU and softplus.
 #pragma once
 
@@ -35,17 +36,17 @@
 namespace ssm {
 
 constexpr int kP16Threads = 128;              // threads per block
-constexpr int kP16Chunk = 32;                 // steps per staged chunk
+constexpr int kP16Chunk = 48;                 // steps per staged chunk
 constexpr int kP16Halo = 8;                   // x steps staged before the chunk (conv history)
-constexpr int kP16Row = kP16Halo + kP16Chunk; // staged row length in elements (80 B)
+constexpr int kP16Row = kP16Halo + kP16Chunk; // staged row length in elements (112 B)
 constexpr int kP16Segs = kP16Chunk / 8;       // 16-byte segments per staged row
 
 template <int NS, int LPC>
 struct P16Smem {
     static constexpr int kCh = kP16Threads / LPC;  // channels per block
     static constexpr int kNSR = NS < 8 ? 8 : NS;   // B / C rows per block of bcr: a multiple of 128 bytes
-    // every tile that a bulk tensor copy fills starts on a 128-byte boundary (rows of 80 bytes: 8 rows
-    // = 640 bytes, and kCh, kNSR are multiples of 8)
+    // every tile that a bulk tensor copy fills starts on a 128-byte boundary (rows of 112 bytes: 8 rows
+    // = 896 bytes, and kCh, kNSR are multiples of 8)
     uint16_t x[2][kCh][kP16Row];               // bf16 u / x, steps c0-8 .. c0+31
     uint16_t dl[2][kCh][kP16Row];              // bf16 delta at [8 + t - c0]
     uint16_t zz[2][kCh][kP16Row];              // bf16 z at [8 + t - c0]

@@ -129,7 +129,7 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream
 // Launch geometry of each kernel kind, used by the host to plan the L split.
 constexpr int kSeqChanPerBlock = 128, kSeqBlocksPerSM = 3, kSeqChunk = 64;
 constexpr int kG4ChanPerBlock = 32, kG4BlocksPerSM = 7, kG4ChunkSteps = 32;
-constexpr int kP16Threads_ = 128, kP16ChunkSteps = 32;  // kScanP16: channels per block = 128 / lpc
+constexpr int kP16Threads_ = 128, kP16ChunkSteps = 48;  // kScanP16: channels per block = 128 / lpc
 
 // Per-dtype-combination entry points defined in scan_<in>_<out>.cu.
 cudaError_t launch_scan_f32_f32(const ScanKernelArgs& a, int zoh, cudaStream_t s);
