@@ -458,6 +458,11 @@ def run_b300(args, rank, world, local):
     hbm = {"achieved_gbs": nbytes / t_s / 1e9, "peak_gbs": hbm_peak, "frac": nbytes / t_s / 1e9 / hbm_peak,
            "bytes_per_launch": nbytes, "peak_source": hbm_src}
 
+    # --- the other scan workloads of the suite (not the headline) ---
+    others = None
+    if not args.no_configs:
+        others = run_other_configs(ssm, dev, args.workload, hbm_peak, fp32_peak, mufu_peak, world)
+
     # --- a training step: forward keeping every state, then the backward pass ---
     backward = None
     if not args.no_backward:
@@ -484,6 +489,7 @@ def run_b300(args, rank, world, local):
             "config": config_dict(cfg, world),
             "gpu_launches": K * launches_per_step,
             "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode, "backward": backward,
+            "other_workloads": others,
             "clocks": clk.summary(), "wall_s_timed_region": wall, "mufu_probe": probe,
             "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
         }
@@ -538,6 +544,62 @@ def run_decode(ssm, dev, hbm_peak, world, steps=None, nlayers=None):
             "tokens_per_s": world * cfg.batch * steps / (ms * 1e-3), "ms_total": ms,
             "us_per_layer_call": ms * 1e3 / calls, "state_cache_gbs": 2 * state_bytes * calls / (ms * 1e-3) / 1e9,
             "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_call": per_call, "launch": "CUDA graph per token"}
+
+
+def run_other_configs(ssm, dev, skip: str, hbm_peak: float, fp32_peak: float, mufu_peak: float, world: int,
+                      steps: int = 20) -> dict:
+    """Every other scan workload of the suite, timed like the headline (L2 flushed between steps, CUDA
+    events, mean of `steps`): time, elements/s and the three roofline fractions.  The long sequence runs
+    as one call with the L split and, as it is also used, as 32 chained calls of 2048 steps."""
+    out = {}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for name, cfg in workloads.SCAN_CONFIGS.items():
+        if name == skip:
+            continue
+        d = workloads.make_scan_inputs(cfg)
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        y = torch.empty_like(g["u"])
+        h = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+        kw = dict(Dskip=g["Dskip"], delta_bias=g["delta_bias"], z=g["z"], conv_w=g["conv_w"], conv_b=g["conv_b"],
+                  zoh=cfg.zoh)
+        ws = ssm.ssm_scan_workspace_size(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h_out=h, y=y, **kw)
+        wsb = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        variants = {"one call": lambda: ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], y=y, h_out=h,
+                                                          workspace=wsb, **kw)}
+        if cfg.chunk:
+            pieces = [{k: g[k][..., a:a + cfg.chunk].contiguous() for k in ("u", "delta", "z", "Bm", "Cm")}
+                      for a in range(0, cfg.seqlen, cfg.chunk)]
+            yp = torch.empty_like(pieces[0]["u"])
+
+            def chained():
+                h.zero_()
+                for pc in pieces:
+                    ssm.ssm_scan_fwd(pc["u"], pc["delta"], g["A"], pc["Bm"], pc["Cm"], h0=h, h_out=h, y=yp,
+                                     **dict(kw, z=pc["z"]))
+            variants[f"{cfg.seqlen // cfg.chunk} chained calls"] = chained
+        res = {}
+        for vname, fn in variants.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(steps):
+                flush.zero_()
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record()
+                fn()
+                b_.record()
+                torch.cuda.synchronize()
+                ts.append(a_.elapsed_time(b_))
+            ms = max_over_ranks(statistics.fmean(ts), world)
+            t_s = ms * 1e-3
+            res[vname] = {"ms": ms, "value": aggregate_rate(cfg.elements, world, ms),
+                          "fp32_frac": scan_fp32_ops(cfg) / t_s / fp32_peak,
+                          "mufu_frac": scan_mufu_ops(cfg) / t_s / mufu_peak,
+                          "hbm_frac": scan_bytes(cfg) / t_s / 1e9 / hbm_peak}
+        out[f"{name}: batch={cfg.batch} d_inner={cfg.dim} d_state={cfg.dstate} L={cfg.seqlen} {cfg.dtype}"] = res
+        del g, d
+    return out
 
 
 def run_backward(ssm, dev, cfg, g, hbm_peak, world, steps=5):
@@ -636,6 +698,7 @@ def main():
                     help="dram bytes per launch from an ncu capture of this kernel (reported as is)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the training-step (backward) measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other scan workloads")
     ap.add_argument("--backward-only", action="store_true", help="run only the training-step measurement")
     ap.add_argument("--decode-only", action="store_true", help="run only the decode workload")
     ap.add_argument("--decode-layers", type=int, default=None, help="decode layers (default 64)")

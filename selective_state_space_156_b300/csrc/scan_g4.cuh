@@ -420,14 +420,14 @@ cudaError_t launch_g4_ns(const ScanKernelArgs& a, cudaStream_t stream) {
     cudaError_t e;
     if (a.nseg > 1) {
         auto kfn = scan_g4_kernel<NSL, kZOH, false, kConv>;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = set_dynamic_smem_once(kfn, (int)smem);
         if (e != cudaSuccess) return e;
         kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     auto kfn = scan_g4_kernel<NSL, kZOH, true, kConv>;
-    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = set_dynamic_smem_once(kfn, (int)smem);
     if (e != cudaSuccess) return e;
     kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a);
     return cudaGetLastError();

@@ -504,7 +504,7 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
     cudaError_t e;
     if (a.nseg > 1) {
         auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv, false, kTma>;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = set_dynamic_smem_once(kfn, (int)smem);
         if (e != cudaSuccess) return e;
         kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a, maps);
         e = cudaGetLastError();
@@ -512,7 +512,7 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
     }
     auto kfn = a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true, kTma>
                                   : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma>;
-    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = set_dynamic_smem_once(kfn, (int)smem);
     if (e != cudaSuccess) return e;
     kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a, maps);
     return cudaGetLastError();

@@ -126,6 +126,19 @@ struct ScanBwdArgs {
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream);
 
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per kernel, size and device, not
+// on every launch (the call costs microseconds of host time; a prefill in chunks launches many times).
+cudaError_t set_dynamic_smem(const void* kernel, int bytes);
+
+// Blocks of `kernel` that the current device keeps resident at once (SMs x occupancy), cached per
+// kernel, launch shape and device.
+cudaError_t resident_blocks(const void* kernel, int threads, int smem_bytes, int* slots);
+
+template <typename K>
+inline cudaError_t set_dynamic_smem_once(K* kernel, int bytes) {
+    return set_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
+}
+
 // Launch geometry of each kernel kind, used by the host to plan the L split.
 constexpr int kSeqChanPerBlock = 128, kSeqBlocksPerSM = 3, kSeqChunk = 64;
 constexpr int kG4ChanPerBlock = 32, kG4BlocksPerSM = 7, kG4ChunkSteps = 32;

@@ -313,14 +313,13 @@ template <typename T, int N, bool kZOH, bool kConv>
 cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
     using L = BulkLayout<T, N, kConv>;
     auto kfn = state_update_bulk_kernel<T, N, kZOH, kConv>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    cudaError_t e = set_dynamic_smem_once(kfn, L::kSmem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kBulkThreads + 32, L::kSmem)) != cudaSuccess) return e;
+    int slots = 0;  // resident blocks on the whole device, asked once per kernel and device
+    if ((e = resident_blocks(reinterpret_cast<const void*>(kfn), kBulkThreads + 32, L::kSmem, &slots)) != cudaSuccess)
+        return e;
     const long long tiles = (long long)a.Bsz * ((a.D + kTileRows - 1) / kTileRows);
-    const int grid = (int)std::min<long long>(tiles, (long long)sms * std::max(per_sm, 1));
+    const int grid = (int)std::min<long long>(tiles, (long long)std::max(slots, 1));
     kfn<<<grid, kBulkThreads + 32, L::kSmem, stream>>>(a);
     return cudaGetLastError();
 }

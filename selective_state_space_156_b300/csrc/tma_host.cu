@@ -1,9 +1,11 @@
 // Host side of the tiled bulk-tensor copies: the driver's tensor-map encoder, looked up once through the
-// runtime so that the library does not link against libcuda.
+// runtime so that the library does not link against libcuda; and the once-per-kernel shared-memory
+// attribute of the kernels that use more than 48 KB.
 #include <mutex>
 
 #include <cudaTypedefs.h>
 
+#include "ssm_internal.h"
 #include "tma.cuh"
 
 namespace ssm {
@@ -39,6 +41,58 @@ bool encode_bf16_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t set_dynamic_smem(const void* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    struct Key {
+        const void* k;
+        int bytes, dev;
+    };
+    static std::mutex mu;
+    static Key seen[256];
+    static int nseen = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < nseen; ++i)
+            if (seen[i].k == kernel && seen[i].bytes == bytes && seen[i].dev == dev) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (nseen < 256) seen[nseen++] = Key{kernel, bytes, dev};
+    return cudaSuccess;
+}
+
+cudaError_t resident_blocks(const void* kernel, int threads, int smem_bytes, int* slots) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    struct Key {
+        const void* k;
+        int threads, smem, dev, slots;
+    };
+    static std::mutex mu;
+    static Key seen[256];
+    static int nseen = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < nseen; ++i)
+            if (seen[i].k == kernel && seen[i].threads == threads && seen[i].smem == smem_bytes && seen[i].dev == dev) {
+                *slots = seen[i].slots;
+                return cudaSuccess;
+            }
+    }
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes)) != cudaSuccess)
+        return e;
+    *slots = sms * per_sm;
+    std::lock_guard<std::mutex> lock(mu);
+    if (nseen < 256) seen[nseen++] = Key{kernel, threads, smem_bytes, dev, *slots};
+    return cudaSuccess;
 }
 
 }  // namespace ssm
