@@ -31,7 +31,7 @@ constexpr int kBwdGroup = 8;    // steps per group (vector loads / stores, one r
 template <int NS>
 struct BwdShared {
     float bc[2][kBwdChunk][NS];               // B_t[n], C_t[n] of the chunk, fp32
-    float tr[kBwdThreads / 32][32][33];       // per-warp transpose of 32 values x 32 lanes (padded)
+    float tr[kBwdThreads / 32][32][36];       // per warp: a row of 32 values per lane (padded to 36)
     float ws[kBwdThreads / 32][kBwdGroup][32];  // per-warp sums of the group's steps
 };
 
@@ -54,13 +54,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     const size_t rowoff = row * (size_t)a.L;
     const int L = a.L, N = a.N;
 
-    // per-channel constants
-    float av[NS], inva[NS];
+    // per-channel constants, as packed pairs of states (n, n + 1)
+    f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2];
+    bool zero_a = false;
 #pragma unroll
-    for (int n = 0; n < NS; ++n) {
-        av[n] = (active && n < N) ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
-        inva[n] = av[n] != 0.0f ? 1.0f / av[n] : 0.0f;
+    for (int p = 0; p < NS / 2; ++p) {
+        float av[2], iv[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int n = 2 * p + q;
+            av[q] = (active && n < N) ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
+            iv[q] = av[q] != 0.0f ? 1.0f / av[q] : 0.0f;
+            zero_a |= active && n < N && av[q] == 0.0f;
+        }
+        a2[p] = pack2(av[0], av[1]);
+        al2[p] = pack2(av[0] * kLog2e, av[1] * kLog2e);
+        inva2[p] = pack2(iv[0], iv[1]);
     }
+    // a block with some A == 0 takes the element-wise form of the zero-order-hold factor (its a -> 0
+    // limit) in every step; the others the packed form
+    const bool safe = kZOH && __syncthreads_or(zero_a);
     float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
     if (kConv && active) {
         const int W = a.conv_width;
@@ -73,11 +86,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     const bool has_z = a.z != nullptr;
 
     // adjoint of the final state, and the per-row gradient accumulators
-    float g[NS], da[NS];
+    f32x2 g2[NS / 2], da2[NS / 2];
 #pragma unroll
-    for (int n = 0; n < NS; ++n) {
-        g[n] = (a.dh_out && active && n < N) ? a.dh_out[row * N + n] : 0.0f;
-        da[n] = 0.0f;
+    for (int p = 0; p < NS / 2; ++p) {
+        float gv[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            gv[q] = (a.dh_out && active && 2 * p + q < N) ? a.dh_out[row * N + 2 * p + q] : 0.0f;
+        g2[p] = pack2(gv[0], gv[1]);
+        da2[p] = pack2(0.0f, 0.0f);
     }
     float dD = 0.0f, dbias = 0.0f, dw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dcb = 0.0f;
     float px[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // pending dx of x_t, x_{t-1}, x_{t-2}, x_{t-3}
@@ -85,9 +102,48 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     // h_t of the step being processed; starts at h_{L-1}
     const size_t hstride = (size_t)a.D * N;  // h_all: (B, L, D, N)
     const float* hrow = a.h_all + ((size_t)b * L * a.D + dd) * N;
-    float hcur[NS];
+    // states as packed pairs; whole 16-byte rows of h_all load as pairs directly
+    const bool hvec = (N == NS) && ((reinterpret_cast<uintptr_t>(a.h_all) & 15) == 0);
+    auto load_h = [&](int t, f32x2 (&hp)[NS / 2]) {
+        if (hvec && active) {
+            const ulonglong2* q = reinterpret_cast<const ulonglong2*>(hrow + (size_t)t * hstride);
 #pragma unroll
-    for (int n = 0; n < NS; ++n) hcur[n] = (active && n < N) ? hrow[(size_t)(L - 1) * hstride + n] : 0.0f;
+            for (int k = 0; k < NS / 4; ++k) {
+                const ulonglong2 w2 = __ldcs(q + k);
+                hp[2 * k] = w2.x;
+                hp[2 * k + 1] = w2.y;
+            }
+        } else {
+#pragma unroll
+            for (int p = 0; p < NS / 2; ++p) {
+                float hv[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    hv[q] = (active && 2 * p + q < N) ? hrow[(size_t)t * hstride + 2 * p + q] : 0.0f;
+                hp[p] = pack2(hv[0], hv[1]);
+            }
+        }
+    };
+    // h_{t}, the state of the step being processed, and a ring of the next two earlier states (h_{t-1},
+    // h_{t-2}) loaded ahead so that the load latency overlaps two steps of work; before t = 0 it is h0
+    auto fetch = [&](int t, f32x2 (&hp)[NS / 2]) {
+        if (t >= 0) {
+            load_h(t, hp);
+        } else {
+#pragma unroll
+            for (int p = 0; p < NS / 2; ++p) {
+                float hv[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    hv[q] = (t == -1 && a.h0 && active && 2 * p + q < N) ? a.h0[row * N + 2 * p + q] : 0.0f;
+                hp[p] = pack2(hv[0], hv[1]);
+            }
+        }
+    };
+    f32x2 hcur[NS / 2], ring0[NS / 2], ring1[NS / 2];
+    load_h(L - 1, hcur);
+    fetch(L - 2, ring0);
+    fetch(L - 3, ring1);
 
     const int last_chunk = ((L - 1) / kBwdChunk) * kBwdChunk;
     for (int c0 = last_chunk; c0 >= 0; c0 -= kBwdChunk) {
@@ -161,27 +217,22 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 }
                 const float s = dv[j] + bias;
                 const float dt = a.softplus ? softplus(s) : s;
-                // h_{t-1}: the previous step's state, or h0 before t = 0
-                float hprev[NS];
-                if (t > 0 && N == NS && active) {  // whole 16-byte rows of h_all
-                    const float4* hp4 = reinterpret_cast<const float4*>(hrow + (size_t)(t - 1) * hstride);
+                // h_{t-1} from the ring; the ring moves on and fetches h_{t-3}
+                f32x2 hprev[NS / 2];
 #pragma unroll
-                    for (int k = 0; k < NS / 4; ++k) {
-                        const float4 q4 = __ldcs(hp4 + k);
-                        hprev[4 * k] = q4.x; hprev[4 * k + 1] = q4.y; hprev[4 * k + 2] = q4.z; hprev[4 * k + 3] = q4.w;
-                    }
-                } else if (t > 0) {
-#pragma unroll
-                    for (int n = 0; n < NS; ++n) hprev[n] = (active && n < N) ? hrow[(size_t)(t - 1) * hstride + n] : 0.0f;
-                } else {
-#pragma unroll
-                    for (int n = 0; n < NS; ++n) hprev[n] = (a.h0 && active && n < N) ? a.h0[row * N + n] : 0.0f;
+                for (int p = 0; p < NS / 2; ++p) {
+                    hprev[p] = ring0[p];
+                    ring0[p] = ring1[p];
                 }
-                const float* Bt = sh.bc[0][t - c0];
-                const float* Ct = sh.bc[1][t - c0];
-                float yss = dsk * v;
+                if (t - 3 >= -1) fetch(t - 3, ring1);
+                const f32x2* Bt = reinterpret_cast<const f32x2*>(sh.bc[0][t - c0]);
+                const f32x2* Ct = reinterpret_cast<const f32x2*>(sh.bc[1][t - c0]);
+                f32x2 yacc = pack2(0.0f, 0.0f);
 #pragma unroll
-                for (int n = 0; n < NS; ++n) yss = fmaf(Ct[n], hcur[n], yss);
+                for (int p = 0; p < NS / 2; ++p) yacc = fma2(Ct[p], hcur[p], yacc);
+                float ya, yb;
+                unpack2(yacc, ya, yb);
+                const float yss = fmaf(dsk, v, ya + yb);
                 float dyss = gy[j];
                 if (has_z) {
                     const float sg = sigmoid_f(zv[j]);
@@ -190,36 +241,54 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     dyss = gy[j] * gz;
                 }
                 dD = fmaf(dyss, v, dD);
-                float dvv = dsk * dyss, ddt = 0.0f;
-                float red[32];
+                const f32x2 dyss2 = pack2(dyss, dyss), dt2 = pack2(dt, dt), v2 = pack2(v, v);
+                const f32x2 one2 = pack2(1.0f, 1.0f);
+                f32x2 dvp = pack2(0.0f, 0.0f), ddtp = pack2(0.0f, 0.0f);
+                f32x2 red2[16];
 #pragma unroll
-                for (int n = 0; n < NS; ++n) {
-                    g[n] = fmaf(Ct[n], dyss, g[n]);
-                    red[16 + n] = dyss * hcur[n];                 // dC contribution
-                    const float x = dt * av[n];
-                    const float Ab = ex2(x * kLog2e);
-                    float E, dEdt, dEda;
-                    if (kZOH) {
-                        const bool nz = av[n] != 0.0f;
-                        E = nz ? (Ab - 1.0f) * inva[n] : dt;
+                for (int p = 0; p < NS / 2; ++p) {
+                    g2[p] = fma2(Ct[p], dyss2, g2[p]);
+                    red2[8 + p] = mul2(dyss2, hcur[p]);                 // dC contribution
+                    const f32x2 Ab = ex2x2(mul2(dt2, al2[p]));
+                    f32x2 E, dEdt, dEda;
+                    if (!kZOH) {
+                        E = dt2;
+                        dEdt = one2;
+                        dEda = pack2(0.0f, 0.0f);
+                    } else if (!safe) {
+                        E = mul2(sub2(Ab, one2), inva2[p]);
                         dEdt = Ab;
-                        dEda = nz ? (dt * Ab - E) * inva[n] : 0.5f * dt * dt;
-                    } else {
-                        E = dt;
-                        dEdt = 1.0f;
-                        dEda = 0.0f;
+                        dEda = mul2(sub2(mul2(dt2, Ab), E), inva2[p]);
+                    } else {  // some A == 0 in the block: the a -> 0 limits E = dt, dE/da = dt^2 / 2
+                        float ab0, ab1, av0, av1, iv0, iv1;
+                        unpack2(Ab, ab0, ab1);
+                        unpack2(a2[p], av0, av1);
+                        unpack2(inva2[p], iv0, iv1);
+                        const float E0 = av0 != 0.0f ? (ab0 - 1.0f) * iv0 : dt;
+                        const float E1 = av1 != 0.0f ? (ab1 - 1.0f) * iv1 : dt;
+                        E = pack2(E0, E1);
+                        dEdt = Ab;
+                        dEda = pack2(av0 != 0.0f ? (dt * ab0 - E0) * iv0 : 0.5f * dt * dt,
+                                     av1 != 0.0f ? (dt * ab1 - E1) * iv1 : 0.5f * dt * dt);
                     }
-                    const float dAb = g[n] * hprev[n];
-                    const float dBb = g[n] * v;
-                    dvv = fmaf(g[n] * E, Bt[n], dvv);
-                    red[n] = dBb * E;                              // dB contribution
-                    const float dE = dBb * Bt[n];
-                    ddt = fmaf(dAb * Ab, av[n], fmaf(dE, dEdt, ddt));
-                    da[n] = fmaf(dAb * Ab, dt, fmaf(dE, dEda, da[n]));
-                    g[n] *= Ab;
+                    const f32x2 dAb = mul2(g2[p], hprev[p]);
+                    const f32x2 dBb = mul2(g2[p], v2);
+                    dvp = fma2(mul2(g2[p], E), Bt[p], dvp);
+                    red2[p] = mul2(dBb, E);                              // dB contribution
+                    const f32x2 dE = mul2(dBb, Bt[p]);
+                    const f32x2 tA = mul2(dAb, Ab);
+                    ddtp = fma2(tA, a2[p], fma2(dE, dEdt, ddtp));
+                    da2[p] = fma2(tA, dt2, fma2(dE, dEda, da2[p]));
+                    g2[p] = mul2(g2[p], Ab);
+                    hcur[p] = hprev[p];
                 }
 #pragma unroll
-                for (int n = NS; n < 16; ++n) red[n] = red[16 + n] = 0.0f;
+                for (int p = NS / 2; p < 8; ++p) red2[p] = red2[8 + p] = pack2(0.0f, 0.0f);
+                float d0, d1;
+                unpack2(dvp, d0, d1);
+                const float dvv = fmaf(dsk, dyss, d0 + d1);
+                unpack2(ddtp, d0, d1);
+                const float ddt = d0 + d1;
                 const float ds = a.softplus ? ddt * sigmoid_f(s) : ddt;
                 dbias += ds;
                 dd_o[j] = ds;
@@ -240,19 +309,20 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 } else {
                     du_o[j] = dvv;
                 }
-#pragma unroll
-                for (int n = 0; n < NS; ++n) hcur[n] = hprev[n];
-                // the warp's sum of each of the 32 values: transpose through shared memory
+                // the warp's sum of each of the 32 values (dB n, dC n): every lane writes its row of 32
+                // with 16-byte stores, every lane then sums one column (rows padded to 36 floats: both
+                // passes are free of bank conflicts)
                 if (!active) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) red[k] = 0.0f;
+                    for (int k = 0; k < 16; ++k) red2[k] = pack2(0.0f, 0.0f);
                 }
+                ulonglong2* trow = reinterpret_cast<ulonglong2*>(&sh.tr[warp][lane][0]);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) sh.tr[warp][k][lane] = red[k];
+                for (int k = 0; k < 8; ++k) trow[k] = make_ulonglong2(red2[2 * k], red2[2 * k + 1]);
                 __syncwarp();
                 float sum = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) sum += sh.tr[warp][lane][k];
+                for (int k = 0; k < 32; ++k) sum += sh.tr[warp][k][lane];
                 sh.ws[warp][j][lane] = sum;
                 __syncwarp();
             }
@@ -290,10 +360,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
 
     if (!active) return;
     // the adjoint before t = 0, and the conv history's gradient
+    float gl[NS], dal[NS];
+#pragma unroll
+    for (int p = 0; p < NS / 2; ++p) {
+        unpack2(g2[p], gl[2 * p], gl[2 * p + 1]);
+        unpack2(da2[p], dal[2 * p], dal[2 * p + 1]);
+    }
     if (a.dh0) {
 #pragma unroll
         for (int n = 0; n < NS; ++n)
-            if (n < N) a.dh0[row * N + n] = g[n];
+            if (n < N) a.dh0[row * N + n] = gl[n];
     }
     if (kConv && a.dconv_init) {
         const int W1 = a.conv_width - 1;
@@ -303,7 +379,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     }
 #pragma unroll
     for (int n = 0; n < NS; ++n)
-        if (n < N) atomicAdd(a.dA + (size_t)dd * N + n, da[n]);
+        if (n < N) atomicAdd(a.dA + (size_t)dd * N + n, dal[n]);
     if (a.dDskip) atomicAdd(a.dDskip + dd, dD);
     if (a.ddelta_bias) atomicAdd(a.ddelta_bias + dd, dbias);
     if (kConv) {
