@@ -210,6 +210,10 @@ SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *del
  *   dDskip, ddelta_bias (D); dconv_w (D, W); dconv_b (D); dconv_init (B, D, W-1); dh0 (B, D, N)
  * dA, dB, dC, dDskip, ddelta_bias, dconv_w and dconv_b are sums over rows and steps: the call zeroes
  * them on `stream` and accumulates.  The outputs must not overlap each other or any input.
+ *   workspace, workspace_bytes: optional device scratch that lets the pass split L across thread
+ *       blocks (the adjoint recurrence is linear: per segment a short summary pass, then every segment
+ *       starts from its exact incoming adjoint), sized by ssm_scan_bwd_workspace_size(); NULL or too
+ *       small runs without the split.  Not to be shared by calls that may run concurrently.
  * dstate 1..16.  Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA.
  */
 typedef struct ssm_scan_bwd_params {
@@ -245,9 +249,15 @@ typedef struct ssm_scan_bwd_params {
     float *dconv_b;
     void *dconv_init;
     float *dh0;
+    void *workspace;
+    size_t workspace_bytes;
 } ssm_scan_bwd_params;
 
 SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream);
+
+/* Bytes of workspace that let ssm_scan_bwd split L for this problem on the current device (0 when no
+   split would be used, or for an invalid p). */
+SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
 
 /*
  * Device-side failures that a kernel could only record, not return.  (No counterpart on the pages.)

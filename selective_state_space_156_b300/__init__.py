@@ -63,7 +63,8 @@ class ScanBwdParams(ctypes.Structure):
         ("du", ctypes.c_void_p), ("ddelta", ctypes.c_void_p), ("dz", ctypes.c_void_p), ("dA", ctypes.c_void_p),
         ("dB", ctypes.c_void_p), ("dC", ctypes.c_void_p), ("dDskip", ctypes.c_void_p),
         ("ddelta_bias", ctypes.c_void_p), ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p),
-        ("dconv_init", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
+        ("dconv_init", ctypes.c_void_p), ("dh0", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
         L.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         L.ssm_scan_bwd.restype = st
         L.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), vp]
+        L.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        L.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
         L.ssm_state_update_conv.restype = st
         L.ssm_state_update_conv.argtypes = [ctypes.POINTER(StepParams), vp]
         L.ssm_device_error.restype = st
@@ -362,10 +365,11 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
                  conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
                  conv_init: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
                  dh_out: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = True,
-                 stream=None) -> dict:
+                 stream=None, workspace="auto") -> dict:
     """Backward pass of ssm_scan_fwd: gradients of sum(y * dy) + sum(h_L * dh_out) for every input, keyed
     like the inputs (``u`` is the gradient of x with a conv; ``h0`` that of the initial state).  ``h_all``
-    (B, L, D, N) fp32 is the forward call's state after every step (ssm_scan_fwd with h_all=...)."""
+    (B, L, D, N) fp32 is the forward call's state after every step (ssm_scan_fwd with h_all=...).
+    ``workspace``: "auto" (allocated here when the L split pays), None (no split) or a uint8 tensor."""
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
     Bsz, D, L = u.shape
@@ -416,5 +420,11 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
     p.dDskip, p.ddelta_bias = _ptr(g["Dskip"], "dDskip"), _ptr(g["delta_bias"], "ddelta_bias")
     p.dconv_w, p.dconv_b = _ptr(g["conv_w"], "dconv_w"), _ptr(g["conv_b"], "dconv_b")
     p.dconv_init, p.dh0 = _ptr(g["conv_init"], "dconv_init"), _ptr(g["h0"], "dh0")
+    if isinstance(workspace, str) and workspace == "auto":
+        n = int(lib().ssm_scan_bwd_workspace_size(ctypes.byref(p)))
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev) if n > 0 else None
+    if workspace is not None:
+        p.workspace = _ptr(workspace, "workspace", torch.uint8)
+        p.workspace_bytes = workspace.numel()
     _check(lib().ssm_scan_bwd(ctypes.byref(p), _stream(stream)))
     return {k: v for k, v in g.items() if v is not None}

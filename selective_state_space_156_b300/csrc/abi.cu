@@ -276,7 +276,42 @@ const char* ssm_last_error(void) { return g_last_error.c_str(); }
 
 const char* ssm_version(void) { return "ssm_b300 0.1 (sm_103a)"; }
 
-ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward's L split: as for the forward (a split only when the (b, channel-block) grid fills less
+// than half the resident block slots, so that the split grid still runs in one wave), with the backward
+// kernel's 128 channels per block and the resident blocks the device reports for the instantiation
+// that will run; segments of a multiple of 64 steps.
+SegPlan bwd_plan(const ssm_scan_bwd_params* p) {
+    const int cpb = 128, chunk = 64;
+    const long long blocks = (long long)((p->dim + cpb - 1) / cpb) * p->batch;
+    int rs = 0;
+    if (ssm::scan_bwd_resident_blocks((int)p->in_dtype, p->dstate, p->zoh, p->conv_w != nullptr, &rs) !=
+            cudaSuccess ||
+        rs <= 0)
+        rs = sm_count() * 2;
+    const long long slots = rs;
+    SegPlan sp{1, ((p->seqlen + chunk - 1) / chunk) * chunk};
+    if (blocks * 2 >= slots) return sp;
+    long long want = slots / blocks;
+    if (want > p->seqlen / 512) want = p->seqlen / 512;
+    if (want > 64) want = 64;
+    if (want <= 1) return sp;
+    const int seg = (int)(((p->seqlen + want - 1) / want + chunk - 1) / chunk) * chunk;
+    sp.seg_len = seg;
+    sp.nseg = (p->seqlen + seg - 1) / seg;
+    return sp;
+}
+
+size_t bwd_workspace_bytes(const ssm_scan_bwd_params* p, const SegPlan& sp) {
+    if (sp.nseg <= 1) return 0;
+    const size_t rows = (size_t)p->batch * p->dim;
+    return (size_t)(sp.nseg - 1) * rows * ((size_t)p->dstate + 1 + 3) * sizeof(float) + 3 * 256;
+}
+
+ssm_status validate_bwd(const ssm_scan_bwd_params* p) {
     const char* who = "ssm_scan_bwd";
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "%s: params is NULL", who);
     if (p->batch <= 0 || p->dim <= 0 || p->dstate <= 0 || p->seqlen <= 0)
@@ -313,6 +348,26 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
             if (&q != &o && overlaps(o.p, o.n, q.p, q.n))
                 return fail(SSM_ERR_INVALID_ARG, "%s: two outputs overlap", who);
     }
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p) {
+    if (validate_bwd(p) != SSM_OK) return 0;
+    return bwd_workspace_bytes(p, bwd_plan(p));
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
+    const char* who = "ssm_scan_bwd";
+    ssm_status vs = validate_bwd(p);
+    if (vs != SSM_OK) return vs;
+    const size_t rows = (size_t)p->batch * p->dim, nbdl = rows * p->seqlen;
+    const size_t eb = esize(p->in_dtype);
+    const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
+    struct Range { const void* p; size_t n; };
     ssm::ScanBwdArgs a{};
     a.Bsz = p->batch; a.D = p->dim; a.N = p->dstate; a.L = p->seqlen;
     a.u = p->u; a.delta = p->delta; a.A = p->A; a.Bm = p->Bm; a.Cm = p->Cm; a.Dskip = p->Dskip;
@@ -330,6 +385,22 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
                      aligned16(p->dy) && aligned16(p->du) && aligned16(p->ddelta) && (!p->z || aligned16(p->z)) &&
                      (!p->z || aligned16(p->dz)) && p->seqlen % 8 == 0;
     a.vec = a16 ? 1 : 0;
+    SegPlan sp = bwd_plan(p);
+    if (sp.nseg > 1 && (p->workspace == nullptr || p->workspace_bytes < bwd_workspace_bytes(p, sp)))
+        sp = SegPlan{1, ((p->seqlen + 63) / 64) * 64};
+    a.nseg = sp.nseg;
+    a.seg_len = sp.seg_len;
+    if (sp.nseg > 1) {
+        uintptr_t base = (reinterpret_cast<uintptr_t>(p->workspace) + 255) & ~(uintptr_t)255;
+        float* w = reinterpret_cast<float*>(base);
+        a.ws_g = w;
+        w += (size_t)(sp.nseg - 1) * rows * p->dstate;
+        w = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(w) + 255) & ~(uintptr_t)255);
+        a.ws_dsum = w;
+        w += (size_t)(sp.nseg - 1) * rows;
+        w = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(w) + 255) & ~(uintptr_t)255);
+        a.ws_pend = w;
+    }
     cudaStream_t st = (cudaStream_t)stream;
     // the accumulated outputs start from zero
     const Range acc[] = {{a.dA, (size_t)p->dim * p->dstate * 4}, {a.dB, nbnl * 4}, {a.dC, nbnl * 4},

@@ -46,13 +46,16 @@ template <typename Tin, int NS, bool kZOH, bool kConv>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs a) {
     __shared__ BwdShared<NS> sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.y;
+    const int b = blockIdx.y, seg = blockIdx.z;
     const int d = blockIdx.x * kBwdThreads + tid;
     const bool active = d < a.D;
     const int dd = active ? d : 0;
     const size_t row = (size_t)b * a.D + dd;
     const size_t rowoff = row * (size_t)a.L;
     const int L = a.L, N = a.N;
+    const size_t rows = (size_t)a.Bsz * a.D;
+    const int t0 = seg * a.seg_len;                // this block's steps: [t0, t1)
+    const int t1 = min(L, t0 + a.seg_len);
 
     // per-channel constants, as packed pairs of states (n, n + 1)
     f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2];
@@ -85,7 +88,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     const float bias = (a.delta_bias && active) ? __ldg(a.delta_bias + dd) : 0.0f;
     const bool has_z = a.z != nullptr;
 
-    // adjoint of the final state, and the per-row gradient accumulators
+    // adjoint of the state at the segment's end: dh_out carried back through the later segments with
+    // their summaries, g <- exp(a sum dt) g + g_local in reverse segment order; and the accumulators
     f32x2 g2[NS / 2], da2[NS / 2];
 #pragma unroll
     for (int p = 0; p < NS / 2; ++p) {
@@ -95,6 +99,17 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
             gv[q] = (a.dh_out && active && 2 * p + q < N) ? a.dh_out[row * N + 2 * p + q] : 0.0f;
         g2[p] = pack2(gv[0], gv[1]);
         da2[p] = pack2(0.0f, 0.0f);
+    }
+    for (int s2 = a.nseg - 1; s2 > seg; --s2) {
+        const float S = active ? a.ws_dsum[(size_t)(s2 - 1) * rows + row] : 0.0f;
+        const float* gl = a.ws_g + ((size_t)(s2 - 1) * rows + row) * N;
+#pragma unroll
+        for (int p = 0; p < NS / 2; ++p) {
+            float gv[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) gv[q] = (active && 2 * p + q < N) ? gl[2 * p + q] : 0.0f;
+            g2[p] = fma2(ex2x2(mul2(pack2(S, S), al2[p])), g2[p], pack2(gv[0], gv[1]));
+        }
     }
     float dD = 0.0f, dbias = 0.0f, dw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dcb = 0.0f;
     float px[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // pending dx of x_t, x_{t-1}, x_{t-2}, x_{t-3}
@@ -141,13 +156,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
         }
     };
     f32x2 hcur[NS / 2], ring0[NS / 2], ring1[NS / 2];
-    load_h(L - 1, hcur);
-    fetch(L - 2, ring0);
-    fetch(L - 3, ring1);
+    load_h(t1 - 1, hcur);
+    fetch(t1 - 2, ring0);
+    fetch(t1 - 3, ring1);
 
-    const int last_chunk = ((L - 1) / kBwdChunk) * kBwdChunk;
-    for (int c0 = last_chunk; c0 >= 0; c0 -= kBwdChunk) {
-        const int clen = min(kBwdChunk, L - c0);
+    const int last_chunk = t0 + ((t1 - 1 - t0) / kBwdChunk) * kBwdChunk;
+    for (int c0 = last_chunk; c0 >= t0; c0 -= kBwdChunk) {
+        const int clen = min(kBwdChunk, t1 - c0);
         __syncthreads();  // everyone is done with the previous chunk's B / C
         for (int i = tid; i < 2 * NS * kBwdChunk; i += kBwdThreads) {
             const int wv = i / (NS * kBwdChunk);
@@ -366,16 +381,23 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
         unpack2(g2[p], gl[2 * p], gl[2 * p + 1]);
         unpack2(da2[p], dal[2 * p], dal[2 * p + 1]);
     }
-    if (a.dh0) {
+    if (a.dh0 && seg == 0) {
 #pragma unroll
         for (int n = 0; n < NS; ++n)
             if (n < N) a.dh0[row * N + n] = gl[n];
     }
-    if (kConv && a.dconv_init) {
+    if (kConv && seg == 0 && a.dconv_init) {
         const int W1 = a.conv_width - 1;
 #pragma unroll
         for (int k = 0; k < 3; ++k)  // px[k] holds dx of x_{-1-k}
             if (k < W1) store1<Tin>(a.dconv_init, row * W1 + W1 - 1 - k, px[k]);
+    }
+    if (kConv && seg > 0) {
+        // the input gradients this segment owes to x_{t0-1}, x_{t0-2}, x_{t0-3} (the previous segment's
+        // steps): added to du by the boundary pass after every segment is done
+        float* pend = a.ws_pend + ((size_t)(seg - 1) * rows + row) * 3;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) pend[k] = px[k];
     }
 #pragma unroll
     for (int n = 0; n < NS; ++n)
@@ -391,11 +413,110 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     }
 }
 
+// Summary of segment s >= 1 for the L split: the adjoint it hands to segment s - 1 when it starts from
+// zero (g <- g + C_t dyss_t, then g <- Abar_t g, back over the segment), and the segment's sum of dt
+// (its decay is exp(a sum dt)).  Needs only dy, z, delta and C: dyss = dy SiLU(z) does not depend on
+// the states.  The final pass folds these in reverse segment order.
+template <typename Tin, int NS>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_summary_kernel(const ScanBwdArgs a) {
+    __shared__ float cs[kBwdChunk][NS];
+    const int tid = threadIdx.x, b = blockIdx.y, seg = blockIdx.z + 1;
+    const int d = blockIdx.x * kBwdThreads + tid;
+    const bool active = d < a.D;
+    const int dd = active ? d : 0;
+    const int L = a.L, N = a.N;
+    const size_t rows = (size_t)a.Bsz * a.D, row = (size_t)b * a.D + dd, rowoff = row * (size_t)L;
+    const int t0 = seg * a.seg_len, t1 = min(L, t0 + a.seg_len);
+    f32x2 al2[NS / 2], g2[NS / 2];
+#pragma unroll
+    for (int p = 0; p < NS / 2; ++p) {
+        float av[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) av[q] = (active && 2 * p + q < N) ? __ldg(a.A + (size_t)dd * N + 2 * p + q) : 0.0f;
+        al2[p] = pack2(av[0] * kLog2e, av[1] * kLog2e);
+        g2[p] = pack2(0.0f, 0.0f);
+    }
+    const float bias = (a.delta_bias && active) ? __ldg(a.delta_bias + dd) : 0.0f;
+    float dsum = 0.0f;
+    const int last_chunk = t0 + ((t1 - 1 - t0) / kBwdChunk) * kBwdChunk;
+    for (int c0 = last_chunk; c0 >= t0; c0 -= kBwdChunk) {
+        const int clen = min(kBwdChunk, t1 - c0);
+        __syncthreads();
+        for (int i = tid; i < NS * kBwdChunk; i += kBwdThreads) {
+            const int n = i / kBwdChunk, t = i - n * kBwdChunk;
+            cs[t][n] = (n < N && t < clen) ? load1<Tin>(a.Cm, ((size_t)b * N + n) * L + c0 + t) : 0.0f;
+        }
+        __syncthreads();
+        for (int g0 = ((clen - 1) / kBwdGroup) * kBwdGroup; g0 >= 0; g0 -= kBwdGroup) {
+            const int tg = c0 + g0, nv = min(kBwdGroup, clen - g0);
+            float dv[kBwdGroup], zv[kBwdGroup], gy[kBwdGroup];
+#pragma unroll
+            for (int j = 0; j < kBwdGroup; ++j) {
+                const bool ok = active && j < nv;
+                dv[j] = ld<Tin>(a.delta, rowoff + tg + j, ok);
+                zv[j] = a.z ? ld<Tin>(a.z, rowoff + tg + j, ok) : 0.0f;
+                gy[j] = ld<Tin>(a.dy, rowoff + tg + j, ok);
+            }
+#pragma unroll
+            for (int j = kBwdGroup - 1; j >= 0; --j) {
+                if (j >= nv) continue;
+                const float sv = dv[j] + bias;
+                const float dt = a.softplus ? softplus(sv) : sv;
+                const float dyss = a.z ? gy[j] * zv[j] * sigmoid_f(zv[j]) : gy[j];
+                const f32x2 dyss2 = pack2(dyss, dyss), dt2 = pack2(dt, dt);
+                const f32x2* Ct = reinterpret_cast<const f32x2*>(cs[tg + j - c0]);
+#pragma unroll
+                for (int p = 0; p < NS / 2; ++p)
+                    g2[p] = mul2(ex2x2(mul2(dt2, al2[p])), fma2(Ct[p], dyss2, g2[p]));
+                dsum += dt;
+            }
+        }
+    }
+    if (!active) return;
+    a.ws_dsum[(size_t)(seg - 1) * rows + row] = dsum;
+    float* gl = a.ws_g + ((size_t)(seg - 1) * rows + row) * N;
+#pragma unroll
+    for (int p = 0; p < NS / 2; ++p) {
+        float g0_, g1_;
+        unpack2(g2[p], g0_, g1_);
+        if (2 * p < N) gl[2 * p] = g0_;
+        if (2 * p + 1 < N) gl[2 * p + 1] = g1_;
+    }
+}
+
+// After the L-split backward: the input gradients each segment s >= 1 owes to the three steps before it
+// (conv taps reaching back over the boundary), added to du there.
+template <typename Tin>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_boundary_kernel(const ScanBwdArgs a) {
+    const int d = blockIdx.x * kBwdThreads + threadIdx.x, b = blockIdx.y, seg = blockIdx.z + 1;
+    if (d >= a.D) return;
+    const size_t rows = (size_t)a.Bsz * a.D, row = (size_t)b * a.D + d;
+    const float* pend = a.ws_pend + ((size_t)(seg - 1) * rows + row) * 3;
+    const int t0 = seg * a.seg_len;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int t = t0 - 1 - k;
+        if (t >= 0) {
+            const size_t i = row * (size_t)a.L + t;
+            store1<Tin>(a.du, i, load1<Tin>(a.du, i) + pend[k]);
+        }
+    }
+}
+
 template <typename Tin, int NS, bool kZOH>
 cudaError_t launch_bwd_z(const ScanBwdArgs& a, cudaStream_t s) {
-    dim3 grid((unsigned)((a.D + kBwdThreads - 1) / kBwdThreads), (unsigned)a.Bsz);
+    const unsigned gx = (unsigned)((a.D + kBwdThreads - 1) / kBwdThreads);
+    if (a.nseg > 1) {
+        scan_bwd_summary_kernel<Tin, NS><<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), kBwdThreads, 0, s>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(gx, (unsigned)a.Bsz, (unsigned)a.nseg);
     if (a.conv_w) scan_bwd_kernel<Tin, NS, kZOH, true><<<grid, kBwdThreads, 0, s>>>(a);
     else scan_bwd_kernel<Tin, NS, kZOH, false><<<grid, kBwdThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.nseg <= 1 || !a.conv_w) return e;
+    scan_bwd_boundary_kernel<Tin><<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), kBwdThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -411,7 +532,27 @@ cudaError_t launch_bwd_t(const ScanBwdArgs& a, int zoh, cudaStream_t s) {
     return launch_bwd_n<Tin, 16>(a, zoh, s);
 }
 
+template <typename Tin, int NS>
+const void* bwd_kernel_ptr(int zoh, bool conv) {
+    if (zoh) return conv ? reinterpret_cast<const void*>(scan_bwd_kernel<Tin, NS, true, true>)
+                         : reinterpret_cast<const void*>(scan_bwd_kernel<Tin, NS, true, false>);
+    return conv ? reinterpret_cast<const void*>(scan_bwd_kernel<Tin, NS, false, true>)
+                : reinterpret_cast<const void*>(scan_bwd_kernel<Tin, NS, false, false>);
+}
+
+template <typename Tin>
+const void* bwd_kernel_ptr_n(int N, int zoh, bool conv) {
+    if (N <= 4) return bwd_kernel_ptr<Tin, 4>(zoh, conv);
+    if (N <= 8) return bwd_kernel_ptr<Tin, 8>(zoh, conv);
+    return bwd_kernel_ptr<Tin, 16>(zoh, conv);
+}
+
 }  // namespace
+
+cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* slots) {
+    const void* k = dtype == 1 ? bwd_kernel_ptr_n<BF16>(N, zoh, conv) : bwd_kernel_ptr_n<F32>(N, zoh, conv);
+    return resident_blocks(k, kBwdThreads, 0, slots);
+}
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream) {
     return dtype == 1 ? launch_bwd_t<BF16>(a, zoh, stream) : launch_bwd_t<F32>(a, zoh, stream);

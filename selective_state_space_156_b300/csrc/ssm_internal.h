@@ -122,9 +122,15 @@ struct ScanBwdArgs {
     float* dh0;
     int softplus;
     int vec;  // every (b, d) row of u / delta / z / dy / du / ddelta / dz is 16-byte aligned and L % 8 == 0
+    int nseg, seg_len;  // L split: segments of seg_len steps (a multiple of 64); 1 = none
+    float* ws_g;        // (nseg - 1, B*D, N) adjoint each segment >= 1 hands back from a zero start
+    float* ws_dsum;     // (nseg - 1, B*D) sum of dt over each segment >= 1
+    float* ws_pend;     // (nseg - 1, B*D, 3) input gradients each segment >= 1 owes to the 3 steps before it
 };
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream);
+// Blocks of the backward kernel a problem of this kind would run that the device keeps resident at once.
+cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* slots);
 
 // cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per kernel, size and device, not
 // on every launch (the call costs microseconds of host time; a prefill in chunks launches many times).

@@ -205,7 +205,8 @@ def test_bwd_params_struct_layout_matches_c():
     got = _c_layout("ssm_scan_bwd_params", """
   F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip) F(delta_bias) F(z)
   F(conv_w) F(conv_b) F(conv_width) F(conv_init) F(h0) F(delta_softplus) F(zoh) F(h_all) F(dy) F(dh_out) F(du)
-  F(ddelta) F(dz) F(dA) F(dB) F(dC) F(dDskip) F(ddelta_bias) F(dconv_w) F(dconv_b) F(dconv_init) F(dh0)""")
+  F(ddelta) F(dz) F(dA) F(dB) F(dC) F(dDskip) F(ddelta_bias) F(dconv_w) F(dconv_b) F(dconv_init) F(dh0)
+  F(workspace) F(workspace_bytes)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanBwdParams)
     assert len(got) == len(ssm.ScanBwdParams._fields_)
     for name, off in got.items():

@@ -31,7 +31,7 @@ def _tol(ref, stored_dtype, in_dtype):
     return k * (np.abs(ref) + rms) + 1e-30
 
 
-def _run(d, dy, dh_out=None):
+def _run(d, dy, dh_out=None, workspace="auto"):
     g = to_dev(d)
     Bsz, D, L = g["u"].shape
     N = g["A"].shape[1]
@@ -42,7 +42,8 @@ def _run(d, dy, dh_out=None):
                      conv_init=g.get("conv_init"), **kw)
     dyd = dy.to(g["u"].dtype).cuda()
     grads = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dyd, h_all, h0=g.get("h0"),
-                             conv_init=g.get("conv_init"), dh_out=None if dh_out is None else dh_out.cuda(), **kw)
+                             conv_init=g.get("conv_init"), dh_out=None if dh_out is None else dh_out.cuda(),
+                             workspace=workspace, **kw)
     torch.cuda.synchronize()
     return grads, dyd.cpu()
 
@@ -130,3 +131,22 @@ def test_backward_at_the_layer_shape_sampled():
         for k in ("A", "Dskip", "delta_bias", "conv_w", "conv_b"):
             got = grads[k][c][None]
             assert_close(got, ref[k], _tol(ref[k], got.dtype, torch.bfloat16), f"d{k} channel {c}")
+
+
+@pytest.mark.parametrize("dt,conv,L", [("bf16", True, 2048), ("f32", False, 3000), ("bf16", True, 1100)])
+def test_backward_with_the_l_split_matches_oracle(dt, conv, L):
+    """Few rows and a long sequence: the pass splits L, summarises every later segment's adjoint and folds
+    it in (and, with the conv, adds the input gradients each segment owes to the steps before it); every
+    gradient against the oracle, and against the same pass without the split."""
+    D, N = 64, 16
+    d = _inputs(1, D, N, L, dt, 9800 + L, conv=conv)
+    gen = torch.Generator().manual_seed(9801)
+    dy = torch.randn((1, D, L), generator=gen).to(d["u"].dtype)
+    dh = torch.randn((1, D, N), generator=gen) * 0.3
+    grads, dyr = _run(d, dy, dh)
+    ref = obwd.scan_bwd(d, dyr, dh)
+    _compare(d, grads, ref, d["u"].dtype)
+    plain, _ = _run(d, dy, dh, workspace=None)
+    for k, v in plain.items():
+        tol = 2e-2 if v.dtype == torch.bfloat16 else 1e-4
+        torch.testing.assert_close(grads[k].float(), v.float(), rtol=tol, atol=tol * float(v.float().abs().max() + 1e-6))
