@@ -58,6 +58,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     return true;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while the previous kernel of the stream drains; pdl_wait blocks until that kernel has completed and
+// its memory is visible (kernels call it before their first global access), pdl_release lets the next
+// such kernel be scheduled.  Both are no-ops for a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // global -> shared bulk copy completing on `bar` (the CTA's own shared memory)
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
     asm volatile(

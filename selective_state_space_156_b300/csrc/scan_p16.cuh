@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
         mbar_init(&tma_bar[1], 1);
         mbar_fence_init();
     }
+    pdl_wait();     // the previous kernel of the stream is done (the summary pass, a previous chunk's call)
+    pdl_release();
     __syncthreads();
     if (kTma) {
         if (tid == 0) p16_tma_chunk<NS, LPC>(maps, sm, &tma_bar[0], 0, row0, brow0, t_begin, has_z);
@@ -506,7 +508,8 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
         auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv, false, kTma>;
         e = set_dynamic_smem_once(kfn, (int)smem);
         if (e != cudaSuccess) return e;
-        kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream>>>(a, maps);
+        e = launch_pdl(kfn, dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream, a, maps);
+        if (e != cudaSuccess) return e;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -514,7 +517,8 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
                                   : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma>;
     e = set_dynamic_smem_once(kfn, (int)smem);
     if (e != cudaSuccess) return e;
-    kfn<<<dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream>>>(a, maps);
+    e = launch_pdl(kfn, dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream, a, maps);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

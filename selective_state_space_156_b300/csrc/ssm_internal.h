@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <string>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -135,6 +136,26 @@ cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* 
 // cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per kernel, size and device, not
 // on every launch (the call costs microseconds of host time; a prefill in chunks launches many times).
 cudaError_t set_dynamic_smem(const void* kernel, int bytes);
+
+// Launch with programmatic stream serialization (the kernel must call pdl_wait before its first global
+// access), unless SSM_PDL=0; then a plain launch.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Blocks of `kernel` that the current device keeps resident at once (SMs x occupancy), cached per
 // kernel, launch shape and device.

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
         }
         mbar_fence_init();
     }
+    pdl_wait();     // the previous kernel of the stream is done: its outputs may be this call's inputs
+    pdl_release();
     __syncthreads();
 
     if (warp == kWarps) {
@@ -320,7 +322,8 @@ cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
         return e;
     const long long tiles = (long long)a.Bsz * ((a.D + kTileRows - 1) / kTileRows);
     const int grid = (int)std::min<long long>(tiles, (long long)std::max(slots, 1));
-    kfn<<<grid, kBulkThreads + 32, L::kSmem, stream>>>(a);
+    e = launch_pdl(kfn, dim3(grid), dim3(kBulkThreads + 32), L::kSmem, stream, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

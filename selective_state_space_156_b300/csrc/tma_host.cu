@@ -1,6 +1,7 @@
 // Host side of the tiled bulk-tensor copies: the driver's tensor-map encoder, looked up once through the
 // runtime so that the library does not link against libcuda; and the once-per-kernel shared-memory
 // attribute of the kernels that use more than 48 KB.
+#include <cstdlib>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -41,6 +42,14 @@ bool encode_bf16_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("SSM_PDL");
+        return !(v != nullptr && v[0] == '0');
+    }();
+    return on;
 }
 
 cudaError_t set_dynamic_smem(const void* kernel, int bytes) {
