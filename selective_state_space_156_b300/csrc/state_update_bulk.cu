@@ -33,7 +33,6 @@ namespace ssm {
 namespace {
 
 constexpr int kBulkThreads = 128;
-constexpr int kTileRows = 64;
 
 __device__ unsigned int g_bulk_wait_error = 0;
 
@@ -41,6 +40,10 @@ constexpr int round16(int x) { return (x + 15) & ~15; }
 
 template <typename T, int N, bool kConv>
 struct BulkLayout {
+    // rows of (b, d) per tile and tiles in flight per block: for N <= 16 two 128-row tiles beat four 64-row
+    // ones (fewer, longer copies per barrier round trip); wider states keep 64-row tiles so that several
+    // blocks still fit on an SM
+    static constexpr int kTileRows = N <= 16 ? 128 : 64;
     static constexpr int kE = T::kBytes;
     static constexpr int kState = kTileRows * N * 4;
     static constexpr int kScal = round16(kTileRows * kE);
@@ -59,7 +62,7 @@ struct BulkLayout {
     static constexpr int kOffCW = kOffCS + (kConv ? round16(kTileRows * 3 * kE) : 0);
     static constexpr int kOffCB = kOffCW + (kConv ? kTileRows * 4 * 4 : 0);
     static constexpr int kBytes = round16(kOffCB + (kConv ? kTileRows * 4 : 0));
-    static constexpr int kStages = N <= 32 ? 4 : 3;
+    static constexpr int kStages = N <= 16 ? 2 : (N <= 32 ? 4 : 3);
     static constexpr int kSmem = 128 + kStages * kBytes;  // barriers and counters first
 };
 
@@ -106,6 +109,7 @@ template <typename T, int N, bool kZOH, bool kConv>
 __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel(const DecodeArgs a) {
     using L = BulkLayout<T, N, kConv>;
     constexpr int S = L::kStages;
+    constexpr int kTileRows = L::kTileRows;
     constexpr int E = L::kE;
     constexpr int TPR = N <= 16 ? 2 : N / 8;   // threads per row
     constexpr int SL = N / TPR;                 // states per thread: 4 (N = 8) or 8
@@ -320,7 +324,7 @@ cudaError_t launch_bulk(const DecodeArgs& a, cudaStream_t stream) {
     int slots = 0;  // resident blocks on the whole device, asked once per kernel and device
     if ((e = resident_blocks(reinterpret_cast<const void*>(kfn), kBulkThreads + 32, L::kSmem, &slots)) != cudaSuccess)
         return e;
-    const long long tiles = (long long)a.Bsz * ((a.D + kTileRows - 1) / kTileRows);
+    const long long tiles = (long long)a.Bsz * ((a.D + L::kTileRows - 1) / L::kTileRows);
     const int grid = (int)std::min<long long>(tiles, (long long)std::max(slots, 1));
     e = launch_pdl(kfn, dim3(grid), dim3(kBulkThreads + 32), L::kSmem, stream, a);
     if (e != cudaSuccess) return e;
