@@ -26,8 +26,9 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ScanConfig", "DecodeConfig", "SCAN_CONFIGS", "DECODE_CONFIG", "make_scan_inputs",
-           "make_decode_layer", "make_decode_pool", "decode_pool_index", "seed_for"]
+__all__ = ["ScanConfig", "DecodeConfig", "SsdConfig", "SCAN_CONFIGS", "DECODE_CONFIG", "SSD_CONFIGS",
+           "make_scan_inputs", "make_decode_layer", "make_decode_pool", "decode_pool_index", "make_ssd_inputs",
+           "seed_for"]
 
 
 @dataclass(frozen=True)
@@ -190,3 +191,78 @@ def make_decode_pool(cfg: DecodeConfig, pool: int, *, device="cpu", batch: Optio
 
 def decode_pool_index(layer: int, step: int, pool: int) -> int:
     return (layer + step) % pool
+
+
+@dataclass(frozen=True)
+class SsdConfig:
+    """A Mamba-2 (SSD) layer: H heads of P channels (d_inner = H * P), one scalar A per head, B and C
+    shared by the H / G heads of each of G groups, state N per channel."""
+    name: str
+    batch: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    seqlen: int
+    has_z: bool = False
+    has_D: bool = True
+    zoh: bool = False
+    seed: int = 2000
+
+    @property
+    def dim(self) -> int:
+        return self.nheads * self.headdim
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.dim * self.seqlen * self.dstate
+
+
+SSD_CONFIGS = {
+    # small: several chunks of 128 steps and a ragged tail, two groups of two heads
+    "ssd_small": SsdConfig("ssd_small", 2, 4, 64, 2, 128, 200, has_z=True, seed=2000),
+    # a Mamba-2 2.7B layer: d_model 2560, expand 2, head dim 64 -> 80 heads, d_state 128, one group
+    "mamba2_2.7b": SsdConfig("mamba2_2.7b", 8, 80, 64, 1, 128, 2048, seed=2001),
+}
+
+
+def make_ssd_inputs(cfg: SsdConfig, *, batch: Optional[int] = None, nheads: Optional[int] = None,
+                    ngroups: Optional[int] = None, seqlen: Optional[int] = None, with_h0: bool = False,
+                    has_z: Optional[bool] = None, seed: Optional[int] = None) -> dict:
+    """CPU tensors for one SSD workload (bf16 x, dt, B, C, z; fp32 A, D skip, dt bias, h0).
+
+      x, z   (B, H * P, L)   channel d = h * P + p, contiguous in L (the Mamba-1 layout)
+      dt     (B, H, L)       raw step of each head, N(0, 0.5^2)
+      A      (H,)            -U[1, 16]
+      Bm, Cm (B, G, L, N)    unit normals; head h reads group h // (H / G)
+      Dskip, dt_bias (H,)    N(0, 1); inverse softplus of dt0 ~ U[1e-3, 1e-1]
+      h0     (B, H, P, N)    N(0, 0.5^2) when asked for
+    """
+    Bsz = cfg.batch if batch is None else batch
+    H = cfg.nheads if nheads is None else nheads
+    G = cfg.ngroups if ngroups is None else ngroups
+    L = cfg.seqlen if seqlen is None else seqlen
+    P, N = cfg.headdim, cfg.dstate
+    base = cfg.seed if seed is None else seed
+    bf = torch.bfloat16
+
+    def normal(tag, shape, std=1.0):
+        t = torch.randn(shape, generator=_gen(base, tag), dtype=torch.float32)
+        return t.mul_(std) if std != 1.0 else t
+
+    z_on = cfg.has_z if has_z is None else has_z
+    return {
+        "x": normal("x", (Bsz, H * P, L)).to(bf),
+        "dt": normal("dt", (Bsz, H, L), 0.5).to(bf),
+        "A": -(1.0 + 15.0 * torch.rand(H, generator=_gen(base, "A"), dtype=torch.float32)),
+        "Bm": normal("B", (Bsz, G, L, N)).to(bf),
+        "Cm": normal("C", (Bsz, G, L, N)).to(bf),
+        "Dskip": normal("D", (H,)) if cfg.has_D else None,
+        "dt_bias": _dt_bias(H, "std", _gen(base, "bias")),
+        "z": normal("z", (Bsz, H * P, L)).to(bf) if z_on else None,
+        "h0": normal("h0", (Bsz, H, P, N), 0.5) if with_h0 else None,
+        "nheads": H,
+        "ngroups": G,
+        "zoh": cfg.zoh,
+        "delta_softplus": True,
+    }
