@@ -266,8 +266,8 @@ SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
  * land (again bounded) and return, leaving the outputs of the affected tiles unwritten and the context
  * usable.  This call
  * synchronises the current device, stores the flags in *flags (0: nothing recorded; bit 0: a decode
- * wait timed out; bit 1: a scan block stopped waiting for its staged chunk, likewise bounded) and
- * clears them.
+ * wait timed out; bit 1: a scan block stopped waiting for its staged chunk, likewise bounded; bit 2: an
+ * SSD block stopped waiting for its copies or its tensor-core products) and clears them.
  * Errors: SSM_ERR_INVALID_ARG (flags NULL), SSM_ERR_CUDA (the synchronisation or the read failed).
  */
 SSM_API ssm_status ssm_device_error(unsigned *flags);
@@ -316,6 +316,55 @@ typedef struct ssm_step_params {
 } ssm_step_params;
 
 SSM_API ssm_status ssm_state_update_conv(const ssm_step_params *p, ssm_stream_t stream);
+
+/*
+ * Mamba-2 (SSD) scan: the selective recurrence with ONE scalar A per head, run by every channel of the
+ * head, with B and C shared by the heads of a group (dpshk.com/news/3333417 sections 6.1 and 6.2;
+ * pwwt.cn/news/5168881 section 2.3).  Per batch row b, head h, channel p of the head and state n, with
+ * g = h / (H / G) the head's group and d = h * P + p its channel:
+ *
+ *   dt_t     = softplus(dt[b,h,t] + dt_bias[h])          (or dt + dt_bias when delta_softplus = 0)
+ *   h_t[p,n] = exp(dt_t A[h]) h_{t-1}[p,n] + w_t B[b,g,t,n] x[b,d,t]
+ *   w_t      = dt_t                       (zoh = 0, the simplified input scale)
+ *            = expm1(dt_t A[h]) / A[h]    (zoh = 1; dt_t at A[h] = 0)
+ *   y[b,d,t] = (sum_n C[b,g,t,n] h_t[p,n] + Dskip[h] x[b,d,t]) * SiLU(z[b,d,t])
+ *
+ * The library evaluates it in its chunked matrix ("dual") form on the tensor cores: per chunk of 128
+ * steps the decayed causal matrix (C B^T masked and scaled) times X, plus the carried state's
+ * contribution, and the chunk's state increment, as bf16 products with fp32 accumulation.
+ *
+ *   x, z, y   (B, H*P, L) bf16    channel d = h*P + p, contiguous in L; z may be NULL (no gate)
+ *   dt        (B, H, L)   bf16    raw step of each head                                   required
+ *   A         (H)         float32 one scalar per head (any finite value)                  required
+ *   Bm, Cm    (B, G, L, N) bf16   contiguous in N                                         required
+ *   Dskip, dt_bias (H)    float32 or NULL
+ *   h0, h_out (B, H, P, N) float32 initial state (NULL: zeros) and final state (NULL: not wanted);
+ *                                 h0 may be the same buffer as h_out
+ * Supported: headdim P = 64, dstate N = 128, ngroups dividing nheads, seqlen % 8 == 0 (the rows of x
+ * are copied by the tensor-memory engine, whose row strides are multiples of 16 bytes), x, Bm and Cm
+ * 16-byte aligned.  y must not overlap any input; h_out must not overlap y or any input but h0.
+ * Errors: SSM_ERR_INVALID_ARG (null params or required pointer, size <= 0, bad flag, overlap),
+ * SSM_ERR_UNSUPPORTED (shape or alignment outside the above), SSM_ERR_CUDA.  A wait for a copy or an
+ * MMA that runs out (about one second) is recorded for ssm_device_error (bit 2).
+ */
+typedef struct ssd_scan_params {
+    int batch, nheads, headdim, ngroups, dstate, seqlen;
+    const void *x;
+    const void *dt;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *Dskip;
+    const float *dt_bias;
+    const void *z;
+    const float *h0;
+    float *h_out;
+    void *y;
+    int delta_softplus;
+    int zoh;
+} ssd_scan_params;
+
+SSM_API ssm_status ssd_scan_fwd(const ssd_scan_params *p, ssm_stream_t stream);
 
 /* Thread-local description of the most recent failed call on this thread ("" if none). */
 SSM_API const char *ssm_last_error(void);

@@ -10,6 +10,8 @@ Entry points (same names as the C ABI):
   causal_conv1d_fwd(x, w, b=None, silu=True)  -> y
   ssm_state_update(state, u, delta, A, Bm, Cm, ...)  -> y  (state updated in place)
   ssm_scan_workspace_size(...)                -> bytes of optional scratch for the L split
+  ssm_scan_bwd(u, delta, A, Bm, Cm, dy, h_all, ...) -> gradients of every input
+  ssd_scan_fwd(x, dt, A, Bm, Cm, nheads=..., ngroups=...) -> y (Mamba-2 / SSD layer, tensor cores)
 """
 from __future__ import annotations
 
@@ -19,8 +21,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_static", "causal_conv1d_fwd", "ssm_state_update", "ssm_scan_workspace_size", "lib",
-           "SsmError", "ScanParams", "LIB_PATH"]
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_static", "causal_conv1d_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+           "ssm_scan_bwd", "ssd_scan_fwd", "lib", "SsmError", "ScanParams", "SsdParams", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssm_b300.so")
 
@@ -109,6 +111,8 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
         L.ssm_state_update_conv.restype = st
         L.ssm_state_update_conv.argtypes = [ctypes.POINTER(StepParams), vp]
+        L.ssd_scan_fwd.restype = st
+        L.ssd_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), vp]
         L.ssm_device_error.restype = st
         L.ssm_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.ssm_last_error.restype = ctypes.c_char_p
@@ -353,7 +357,7 @@ def ssm_state_update(state: torch.Tensor, u: torch.Tensor, delta: torch.Tensor, 
 def ssm_device_error() -> int:
     """Synchronises the current device and returns (and clears) the flags that kernels record when a
     bounded wait runs out: 0 when nothing was recorded, bit 0 for a decode-kernel wait, bit 1 for a scan
-    kernel's wait for its staged chunk."""
+    kernel's wait for its staged chunk, bit 2 for an SSD kernel's wait for its copies or products."""
     flags = ctypes.c_uint(0)
     _check(lib().ssm_device_error(ctypes.byref(flags)))
     return int(flags.value)
@@ -428,3 +432,55 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
         p.workspace_bytes = workspace.numel()
     _check(lib().ssm_scan_bwd(ctypes.byref(p), _stream(stream)))
     return {k: v for k, v in g.items() if v is not None}
+
+
+class SsdParams(ctypes.Structure):
+    """Mirror of ``ssd_scan_params`` in include/ssm_scan.h."""
+    _fields_ = [("batch", ctypes.c_int), ("nheads", ctypes.c_int), ("headdim", ctypes.c_int),
+                ("ngroups", ctypes.c_int), ("dstate", ctypes.c_int), ("seqlen", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("A", ctypes.c_void_p), ("Bm", ctypes.c_void_p),
+                ("Cm", ctypes.c_void_p), ("Dskip", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("z", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("h_out", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int)]
+
+
+def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor, *,
+                 nheads: int, ngroups: int = 1, Dskip: Optional[torch.Tensor] = None,
+                 dt_bias: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                 h0: Optional[torch.Tensor] = None, return_state: bool = False, h_out: Optional[torch.Tensor] = None,
+                 y: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = False, stream=None):
+    """Mamba-2 (SSD) layer scan: x, z (B, H*P, L) bf16; dt (B, H, L) bf16; A, Dskip, dt_bias (H,) fp32;
+    Bm, Cm (B, G, L, N) bf16; h0 / h_out (B, H, P, N) fp32.  Returns y (and the final state with
+    ``return_state``).  Head h reads group h // (H / G)."""
+    if x.dim() != 3:
+        raise ValueError("x must be (batch, nheads * headdim, seqlen)")
+    Bsz, D, L = x.shape
+    H, G = int(nheads), int(ngroups)
+    if H <= 0 or G <= 0 or D % H:
+        raise ValueError("x's channel count must be a multiple of nheads")
+    P = D // H
+    if Bm.dim() != 4:
+        raise ValueError("Bm must be (batch, ngroups, seqlen, dstate)")
+    N = Bm.shape[3]
+    bf = torch.bfloat16
+    if y is None:
+        y = torch.empty_like(x)
+    if return_state and h_out is None:
+        h_out = torch.empty((Bsz, H, P, N), dtype=torch.float32, device=x.device)
+    p = SsdParams()
+    p.batch, p.nheads, p.headdim, p.ngroups, p.dstate, p.seqlen = Bsz, H, P, G, N, L
+    p.x = _ptr(x, "x", bf)
+    p.dt = _ptr(dt, "dt", bf, (Bsz, H, L))
+    p.A = _ptr(A, "A", torch.float32, (H,))
+    p.Bm = _ptr(Bm, "Bm", bf, (Bsz, G, L, N))
+    p.Cm = _ptr(Cm, "Cm", bf, (Bsz, G, L, N))
+    p.Dskip = _ptr(Dskip, "Dskip", torch.float32, (H,))
+    p.dt_bias = _ptr(dt_bias, "dt_bias", torch.float32, (H,))
+    p.z = _ptr(z, "z", bf, (Bsz, D, L))
+    p.h0 = _ptr(h0, "h0", torch.float32, (Bsz, H, P, N))
+    p.h_out = _ptr(h_out, "h_out", torch.float32, (Bsz, H, P, N))
+    p.y = _ptr(y, "y", bf, (Bsz, D, L))
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    _check(lib().ssd_scan_fwd(ctypes.byref(p), _stream(stream)))
+    return (y, h_out) if return_state else y

@@ -419,12 +419,14 @@ ssm_status ssm_device_error(unsigned* flags) {
     if (flags == nullptr) return fail(SSM_ERR_INVALID_ARG, "ssm_device_error: flags is NULL");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: cudaDeviceSynchronize");
-    unsigned dec = 0, scan = 0;
+    unsigned dec = 0, scan = 0, ssd = 0;
     e = ssm::take_bulk_wait_error(&dec);
     if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: reading the decode flag");
     e = ssm::take_scan_wait_error(&scan);
     if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: reading the scan flag");
-    *flags = (dec ? 1u : 0u) | (scan ? 2u : 0u);
+    e = ssm::take_ssd_wait_error(&ssd);
+    if (e != cudaSuccess) return cuda_status(e, "ssm_device_error: reading the SSD flag");
+    *flags = (dec ? 1u : 0u) | (scan ? 2u : 0u) | (ssd ? 4u : 0u);
     return SSM_OK;
 }
 
@@ -581,6 +583,53 @@ ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
         a.ws_h0 = p->h0 != nullptr ? a.ws_h + (size_t)(sp.nseg - 1) * rows * p->dstate : nullptr;
     }
     return launch_scan_and_history(a, p, stream, "ssm_scan_fwd_static launch");
+}
+
+ssm_status ssd_scan_fwd(const ssd_scan_params* p, ssm_stream_t stream) {
+    const char* who = "ssd_scan_fwd";
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "%s: params is NULL", who);
+    if (p->batch <= 0 || p->nheads <= 0 || p->headdim <= 0 || p->ngroups <= 0 || p->dstate <= 0 || p->seqlen <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: sizes must be positive (batch=%d nheads=%d headdim=%d ngroups=%d "
+                    "dstate=%d seqlen=%d)", who, p->batch, p->nheads, p->headdim, p->ngroups, p->dstate, p->seqlen);
+    if (!p->x || !p->dt || !p->A || !p->Bm || !p->Cm || !p->y)
+        return fail(SSM_ERR_INVALID_ARG, "%s: x, dt, A, Bm, Cm and y are required", who);
+    if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->zoh != 0 && p->zoh != 1))
+        return fail(SSM_ERR_INVALID_ARG, "%s: delta_softplus and zoh must be 0 or 1", who);
+    if (p->nheads % p->ngroups != 0)
+        return fail(SSM_ERR_INVALID_ARG, "%s: ngroups %d does not divide nheads %d", who, p->ngroups, p->nheads);
+    if (!ssm::ssd_tc_supported(p->dstate, p->headdim))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: headdim %d / dstate %d not supported (64 / 128)", who, p->headdim,
+                    p->dstate);
+    if (p->seqlen % 8 != 0)
+        return fail(SSM_ERR_UNSUPPORTED, "%s: seqlen %d is not a multiple of 8", who, p->seqlen);
+    if (!aligned16(p->x) || !aligned16(p->Bm) || !aligned16(p->Cm))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: x, Bm and Cm must be 16-byte aligned", who);
+    const size_t B = (size_t)p->batch, H = (size_t)p->nheads, L = (size_t)p->seqlen;
+    const size_t D = H * (size_t)p->headdim, N = (size_t)p->dstate, G = (size_t)p->ngroups;
+    if (B * H > 0x7fffffffu || B * D > 0x7fffffffu || B * G * L * N > ((size_t)1 << 40))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: problem too large", who);
+    const size_t xb = B * D * L * 2, db = B * H * L * 2, bcb = B * G * L * N * 2, hb = B * D * N * 4;
+    struct Span {
+        const void* p;
+        size_t n;
+    };
+    const Span in[] = {{p->x, xb}, {p->dt, db}, {p->A, H * 4}, {p->Bm, bcb}, {p->Cm, bcb}, {p->Dskip, H * 4},
+                       {p->dt_bias, H * 4}, {p->z, xb}, {p->h0, hb}};
+    for (const Span& i : in)
+        if (overlaps(p->y, xb, i.p, i.n)) return fail(SSM_ERR_INVALID_ARG, "%s: y overlaps an input", who);
+    if (p->h_out) {
+        if (overlaps(p->h_out, hb, p->y, xb)) return fail(SSM_ERR_INVALID_ARG, "%s: h_out overlaps y", who);
+        for (const Span& i : in)
+            if (i.p != p->h0 && overlaps(p->h_out, hb, i.p, i.n))
+                return fail(SSM_ERR_INVALID_ARG, "%s: h_out overlaps an input", who);
+        if (p->h0 && p->h0 != p->h_out && overlaps(p->h_out, hb, p->h0, hb))
+            return fail(SSM_ERR_INVALID_ARG, "%s: h_out partly overlaps h0", who);
+    }
+    ssm::SsdArgs a{p->batch, p->nheads, p->ngroups, p->seqlen, p->x, p->dt, p->A, p->Bm, p->Cm, p->Dskip,
+                   p->dt_bias, p->z, p->h0, p->h_out, p->y, p->delta_softplus, p->zoh};
+    cudaError_t e = ssm::launch_ssd_chunked(a, (cudaStream_t)stream);
+    if (e == cudaErrorInvalidValue) return fail(SSM_ERR_UNSUPPORTED, "%s: tensor map encoding refused the layout", who);
+    return cuda_status(e, "ssd_scan_fwd launch");
 }
 
 }  // extern "C"

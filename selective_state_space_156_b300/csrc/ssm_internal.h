@@ -133,6 +133,28 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream
 // Blocks of the backward kernel a problem of this kind would run that the device keeps resident at once.
 cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* slots);
 
+// The Mamba-2 (SSD) chunked scan on the tensor cores (ssd_tc.cu), after host-side validation.
+struct SsdArgs {
+    int Bsz, H, G, L;          // batch, heads, groups, steps; head dim 64 and state 128 (ssd_tc_supported)
+    const void* x;             // (B, H*64, L) bf16
+    const void* dt;            // (B, H, L) bf16
+    const float* A;            // (H)
+    const void* Bm;            // (B, G, L, 128) bf16
+    const void* Cm;            // (B, G, L, 128) bf16
+    const float* Dskip;        // (H) or NULL
+    const float* dt_bias;      // (H) or NULL
+    const void* z;             // (B, H*64, L) bf16 or NULL
+    const float* h0;           // (B, H, 64, 128) or NULL
+    float* h_out;              // (B, H, 64, 128) or NULL
+    void* y;                   // (B, H*64, L) bf16
+    int softplus, zoh;
+};
+
+bool ssd_tc_supported(int N, int P);
+cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream);
+// The SSD kernel's flag for a copy or MMA it stopped waiting for.
+cudaError_t take_ssd_wait_error(unsigned* flags);
+
 // cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per kernel, size and device, not
 // on every launch (the call costs microseconds of host time; a prefill in chunks launches many times).
 cudaError_t set_dynamic_smem(const void* kernel, int bytes);

@@ -22,6 +22,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -29,5 +36,11 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
 // Host: the driver's encoder, looked up once through the runtime (no link against libcuda).
 bool encode_bf16_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
                         uint32_t box_inner, uint32_t box_rows);
+
+// A bf16 tensor of `rank` (2 or 3) dimensions, innermost first (dims[0] contiguous), strides in bytes of
+// dimensions 1.. (multiples of 16), a box of box[0..rank) elements written to shared memory in the
+// 128-byte swizzle layout (box[0] * 2 <= 128 bytes; the destination 1024-byte aligned).
+bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box);
 
 }  // namespace ssm

@@ -44,6 +44,27 @@ bool encode_bf16_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box) {
+    auto fn = encoder();
+    if (fn == nullptr || rank < 2 || rank > 3) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || box[0] * 2 > 128 || (box[0] * 2) % 16 != 0) return false;
+    cuuint64_t d[3], st[2];
+    cuuint32_t bx[3], es[3];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) {
+        if (strides_bytes[i] % 16 != 0) return false;
+        st[i] = strides_bytes[i];
+    }
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* v = std::getenv("SSM_PDL");
