@@ -43,6 +43,7 @@ WORKLOAD = "mamba1.4b_conv"
 METRIC = "scan elems/s (B*D*L*N)"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 MAX_SM_MHZ = 2032.0
 FP32_LANES_PER_SM = 128   # FP32 FMA lanes per SM (4 sub-partitions x 32)
 E2E_TWO_UPLOAD_STREAMS = os.environ.get("SSM_BENCH_E2E_UPLOAD_STREAMS", "2") != "1"
@@ -296,6 +297,13 @@ def run_b300(args, rank, world, local):
         if rank == 0:
             print(json.dumps({"backward": out}), flush=True)
         return
+    if args.ssd_only:  # the Mamba-2 (SSD) layer alone (profiling runs)
+        pk = measured_peaks()
+        ssd = run_ssd(ssm, dev, pk.get("hbm_gbs") or FALLBACK_HBM_GBS, pk.get("bf16_tflops") or FALLBACK_BF16_TFLOPS,
+                      world, steps=max(args.steps, 1))
+        if rank == 0:
+            print(json.dumps({"ssd": ssd}), flush=True)
+        return
     if args.decode_only:  # the decode workload alone (profiling runs; smaller with --decode-layers/steps)
         hbm_peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
         decode = run_decode(ssm, dev, hbm_peak, world, steps=args.decode_steps, nlayers=args.decode_layers)
@@ -483,6 +491,12 @@ def run_b300(args, rank, world, local):
     if not args.no_decode:
         decode = run_decode(ssm, dev, hbm_peak, world, steps=args.decode_steps, nlayers=args.decode_layers)
 
+    # --- Mamba-2 (SSD) layer on the tensor cores ---
+    ssd = None
+    if not args.no_ssd:
+        pk = measured_peaks()
+        ssd = run_ssd(ssm, dev, hbm_peak, pk.get("bf16_tflops") or FALLBACK_BF16_TFLOPS, world)
+
     # --- CPU baseline: oracle on host cores, rank 0 at N = 1 only ---
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -499,6 +513,7 @@ def run_b300(args, rank, world, local):
             "config": config_dict(cfg, world),
             "gpu_launches": K * launches_per_step,
             "roofline": roof, "hbm": hbm, "cpu_baseline": cpu, "e2e": e2e, "decode": decode, "backward": backward,
+            "ssd": ssd,
             "other_workloads": others,
             "clocks": clk.summary(), "wall_s_timed_region": wall, "mufu_probe": probe,
             "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
@@ -612,6 +627,57 @@ def run_other_configs(ssm, dev, skip: str, hbm_peak: float, fp32_peak: float, mu
     return out
 
 
+def run_ssd(ssm, dev, hbm_peak, tensor_peak, world, steps=20):
+    """The Mamba-2 (SSD) layer on the tensor cores: 8 x 80 heads x 64 channels x 128 states x 2048 steps,
+    bf16, one group.  Inputs per rank are drawn from the rank's seed; a 256 MB buffer is written between
+    timed launches (outside the events) so that every launch reads its inputs from HBM.  Roofline terms:
+    the chunked algorithm's dense products (per 128-step chunk and head: C B^T, C S, M X and the state
+    increment, without the hi/lo repeats the kernel adds for precision) against the measured bf16 tensor
+    peak, and the bytes it must move (x, dt, B, C in; y out) against the measured HBM bandwidth."""
+    cfg = workloads.SSD_CONFIGS["mamba2_2.7b"]
+    rank = int(os.environ.get("RANK", "0"))
+    d = workloads.make_ssd_inputs(cfg, seed=cfg.seed + 7919 * rank)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    y = torch.empty_like(g["x"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        ssm.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["Bm"], g["Cm"], nheads=cfg.nheads, ngroups=cfg.ngroups,
+                         Dskip=g["Dskip"], dt_bias=g["dt_bias"], y=y)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = max_over_ranks(statistics.median(times), world)
+    flags = ssm.ssm_device_error()
+    Bsz, D, L = g["x"].shape
+    H, G, P, N, Q = cfg.nheads, cfg.ngroups, cfg.headdim, cfg.dstate, 128
+    chunks = (L + Q - 1) // Q
+    flops = 2.0 * Bsz * H * chunks * (Q * Q * N + Q * N * P + Q * Q * P + N * Q * P)
+    byts = 2 * Bsz * D * L * 2 + Bsz * H * L * 2 + 2 * Bsz * G * L * N * 2
+    t_tensor = flops / (tensor_peak * 1e12) * 1e3
+    t_hbm = byts / (hbm_peak * 1e9) * 1e3
+    return {"workload": f"{cfg.name}: batch {Bsz}, {H} heads x {P}, d_state {N}, {G} group, L {L}, bf16 "
+                        "(ssd_scan_fwd, chunks of 128 on tcgen05)",
+            "ms": ms, "ms_min": min(times), "elements_per_s": world * Bsz * D * L * N / (ms * 1e-3),
+            "tokens_per_s": world * Bsz * L / (ms * 1e-3),
+            "tensor_tflops": flops / (ms * 1e-3) / 1e12, "tensor_peak_tflops": tensor_peak,
+            "tensor_frac": t_tensor / ms, "hbm_gbs": byts / (ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm_peak,
+            "hbm_frac": t_hbm / ms, "roofline_frac": max(t_tensor, t_hbm) / ms,
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+            "flops_per_launch": flops, "bytes_per_launch": byts, "steps": steps, "device_error_flags": flags,
+            "peaks": "of measured (MEASURED_PEAKS.json: bf16 burst, HBM copy)"}
+
+
 def run_backward(ssm, dev, cfg, g, hbm_peak, world, steps=5):
     """A training step of the layer: the forward that keeps the state after every step (h_all, (B, L, D, N)
     fp32), then ssm_scan_bwd over it.  Reported beside the forward-only headline, with the HBM bytes each
@@ -711,6 +777,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other scan workloads")
     ap.add_argument("--backward-only", action="store_true", help="run only the training-step measurement")
     ap.add_argument("--decode-only", action="store_true", help="run only the decode workload")
+    ap.add_argument("--no-ssd", action="store_true", help="skip the Mamba-2 (SSD) layer")
+    ap.add_argument("--ssd-only", action="store_true", help="run only the Mamba-2 (SSD) layer")
     ap.add_argument("--decode-layers", type=int, default=None, help="decode layers (default 64)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode tokens (default 128)")
     ap.add_argument("--no-cpu", action="store_true")

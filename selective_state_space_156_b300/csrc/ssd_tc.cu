@@ -3,20 +3,30 @@
 // section 2.3: the semiseparable matrix splits into blocks that are processed like attention tiles).
 //
 // One CTA owns one (batch row b, head h) and walks its sequence in chunks of Q = 128 steps, carrying the
-// state S (N x P, fp32, in registers: thread n holds row n).  With a_t = exp(dt_t A) and
-// s_i = sum_{t0 <= j <= i} dt_j A (log2 units in the code), per chunk:
+// state S (N x P, fp32, in registers: row n of S belongs to the threads of TMEM lane n).  With
+// a_t = exp(dt_t A) and s_i = sum_{t0 <= j <= i} dt_j A (log2 units in the code), per chunk:
 //
-//   G     = C B^T                                (Q x Q, over the N states)           tensor cores
-//   M     = G o [j <= i] exp(s_i - s_j) w_j      (the decayed causal mask)            threads -> smem
-//   Y     = exp(s_i) (C S) + M X                 (inter-chunk + intra-chunk)          tensor cores
-//   S    <- exp(s_end) S + (exp(s_end - s_j) w_j B_j)^T X                              tensor cores
-//   y     = (Y + Dskip x) * SiLU(z)
+//   [G | C S]  = C [B ; S^T]^T                    (Q x (Q + P) over the N states)        tensor cores
+//   M          = G o [j <= i] exp(s_i - s_j) w_j  + Dskip I                              threads -> smem
+//   Y          = exp(s_i) (C S) + M X              (inter-chunk + intra-chunk + skip)    tensor cores
+//   S         <- exp(s_end) S + B^T (v o X)^T,    v_j = exp(s_end - s_j) w_j             tensor cores
+//   y          = Y * SiLU(z)
 //
-// where w_j = dt_j (simplified input scale) or expm1(dt_j A) / A (zero-order hold), C, B (Q x N) and X
-// (the head's P channels over the chunk) arrive by TMA in the 128-byte swizzle layout, and the operands
-// built by threads (M, the scaled B^T, S^T) are written in the same layout as hi + lo bf16 pairs.
-// Accumulators live in TMEM: G in columns 0..127 (then the state increment in 0..63), C S in 128..191,
-// M X in 192..255.
+// where w_j = dt_j (simplified input scale) or expm1(dt_j A) / A (zero-order hold).  C, B (Q x N) and X
+// (the head's P channels over the chunk) arrive by TMA in the 128-byte swizzle layout; the increment reads
+// B as it landed, as an MN-major operand.  The operands the threads build (M, v o X, S^T) are written in
+// the same layout as two bf16 terms, hi = bf16(u) and lo = bf16(u - hi), and every product with them is
+// issued for both terms into one accumulator, so their rounding costs about 2^-16 relative instead of
+// 2^-8.  S^T's two terms sit right below B in the same K blocks, which makes G and C S one N = 256
+// product per K step.
+//
+// Accumulators in TMEM: G in columns 0..127, C S_hi in 128..191, C S_lo in 192..255, M X in 256..319 and
+// the state increment in 320..383; the increment is issued as soon as v o X is built and runs while the
+// threads build M.  A dedicated warp issues the copies and the products; the
+// element-wise work is split over the compute warpgroups (each warp reads the TMEM lanes of its quarter
+// of the rows).  A chunk's C is fetched as soon as the previous chunk's first product is done, its B and
+// X as soon as the previous M X and increment are; dt is read a chunk ahead; y leaves through a TMA store
+// of the tile staged in M's place.
 #include <cstdint>
 
 #include "bulk_copy.cuh"
@@ -32,35 +42,46 @@ namespace {
 constexpr int kQ = 128;   // chunk length
 constexpr int kN = 128;   // state size
 constexpr int kP = 64;    // channels per head
-constexpr int kThreads = 128;
+#ifndef SSD_COMPUTE_WARPGROUPS
+#define SSD_COMPUTE_WARPGROUPS 4
+#endif
+constexpr int kWG = SSD_COMPUTE_WARPGROUPS;  // compute warpgroups
+constexpr int kCompute = 128 * kWG;          // compute threads
+constexpr int kIssuer = 4 * kWG;             // the warp that issues copies and products
+constexpr int kThreads = kCompute + 32;
 
-// shared memory, from a 1024-byte-aligned base.  The operands built by threads are each stored as two
-// bf16 terms, hi = bf16(v) and lo = bf16(v - hi), and every product with them is issued twice into the
-// same accumulator: the rounding of those operands then costs about 2^-16 relative instead of 2^-8.
-constexpr int kOffC = 0;                        // C chunk: Q rows (t) x N (n), two K blocks of 16 KB
-constexpr int kOffB = kOffC + kQ * kN * 2;      // B chunk, the same shape; once G = C B^T and the scaled
-constexpr int kOffMlo = kOffB;                  //   B^T are built, the lo term of M takes its place
-constexpr int kOffX = kOffB + kQ * kN * 2;      // X chunk: P rows (p) x Q (t), two K blocks of 8 KB
-constexpr int kOffM = kOffX + kP * kQ * 2;      // M (hi): Q rows (i) x Q (j)
-constexpr int kOffBt = kOffM + kQ * kQ * 2;     // scaled B^T (hi): N rows (n) x Q (t)
-constexpr int kOffBtLo = kOffBt + kN * kQ * 2;  // scaled B^T (lo)
-constexpr int kOffSt = kOffBtLo + kN * kQ * 2;  // S^T (hi): P rows (p) x N (n)
-constexpr int kOffStLo = kOffSt + kP * kN * 2;  // S^T (lo)
-constexpr int kOffS2 = kOffStLo + kP * kN * 2;  // float s[Q]: cumulative log2 decay
-constexpr int kOffW = kOffS2 + kQ * 4;          // float w[Q]: input scale
-constexpr int kOffV = kOffW + kQ * 4;           // float v[Q]: exp2(s_end - s_j) w_j
-constexpr int kOffWarp = kOffV + kQ * 4;        // float[4]: warp totals of the prefix sum
-constexpr int kOffBar = kOffWarp + 16;          // uint64 tma barrier, mma barrier
-constexpr int kOffTmem = kOffBar + 16;          // uint32 TMEM base
+// Shared memory, from a 1024-byte-aligned base.  Tiles are 128-byte swizzled in K blocks of 64 elements;
+// swz() gives the byte offset of (row, k) for a K-block stride.
+constexpr int kOffC = 0;                         // C: Q rows (t) x N, K blocks of 16 KB
+constexpr int kBS = 32768;                       // K-block stride of the [B ; S^T hi ; S^T lo] operand:
+constexpr int kOffBS = kOffC + 2 * 16384;        //   rows 0..127 B (t x n), 128..191 S^T hi and 192..255
+constexpr int kRowStHi = 128, kRowStLo = 192;    //   S^T lo (p x n)
+constexpr int kOffX = kOffBS + 2 * kBS;          // X: P rows (p) x Q (t), K blocks of 8 KB
+constexpr int kOffXs = kOffX + 2 * 8192;         // v o X hi, the same shape
+constexpr int kOffXsLo = kOffXs + 2 * 8192;      // v o X lo
+constexpr int kOffM = kOffXsLo + 2 * 8192;       // M hi: Q rows (i) x Q (j), K blocks of 16 KB; then the
+                                                 //   y tile (p x t, K blocks of 8 KB)
+constexpr int kOffMlo = kOffM + 2 * 16384;       // M lo
+constexpr int kOffS2 = kOffMlo + 2 * 16384;      // float s[Q]: cumulative log2 decay
+constexpr int kOffW = kOffS2 + kQ * 4;           // float w[Q]: input scale
+constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j) w_j
+constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
+constexpr int kOffBar = kOffWarp + 16;           // uint64 barriers: C landed, B and X landed, products done
+constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base
 constexpr int kSmemUsed = kOffTmem + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
+constexpr int kSmemBytes = kSmemUsed + 1024;     // slack for aligning the base
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0, kColSc = 0, kColY1 = 128, kColY2 = 192;
-constexpr unsigned kTileBytes = 2 * kQ * kN * 2 + kP * kQ * 2;   // C + B + X per chunk
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0, kColY1 = 128, kColY2 = 256, kColSc = 320;
+constexpr unsigned kCBytes = kQ * kN * 2, kBBytes = kQ * kN * 2, kXBytes = kP * kQ * 2;   // per chunk
 
 __device__ unsigned int g_ssd_wait_error = 0;
+
+__host__ __device__ constexpr uint32_t swz(int kb_stride, int row, int k) {
+    return static_cast<uint32_t>((k >> 6) * kb_stride + row * 128 + ((((k >> 3) & 7) ^ (row & 7)) << 4) +
+                                 ((k & 7) << 1));
+}
 
 // every thread waits; false on every thread if any of them gave up
 __device__ __forceinline__ bool wait_all(uint64_t* bar, unsigned parity) {
@@ -73,277 +94,371 @@ __device__ __forceinline__ void st_shared_v4(unsigned char* p, uint32_t a, uint3
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_u32(unsigned char* p, uint32_t a) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const unsigned char* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
 // two floats as a bf16x2 hi word and the bf16x2 word of what hi leaves over
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
     hi = pack_bf16x2(a, b);
     lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
 }
 
-__device__ __forceinline__ float ld_bf16_shared(const unsigned char* p) {
-    return bf16_to_f32(*reinterpret_cast<const uint16_t*>(p));
+// Lanes r and r ^ 1 hold the same columns of rows r and r ^ 1 of a row-per-lane matrix; the transposed
+// tile wants (column, row pair) words.  For the column pair (c, c + 1) the even lane returns the pair of
+// rows (r, r + 1) of column c, the odd lane that of column c + 1, and `col` tells which.
+__device__ __forceinline__ void pair_rows(float own_c, float own_c1, int odd, float& first, float& second) {
+    const float recv = __shfl_xor_sync(0xffffffffu, odd ? own_c : own_c1, 1);
+    first = odd ? recv : own_c;
+    second = odd ? own_c1 : recv;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_x) {
+                     const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_y) {
+    constexpr int kPW = kP / kWG;   // channels p whose outputs and state each compute warpgroup owns
+    static_assert(kPW % 16 == 0, "warpgroup split");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     unsigned char* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer_warp = warp == kIssuer;
+    const bool issuer = issuer_warp && lane == 0;
+    const int r = tid & 127;        // compute threads: TMEM lane, step i of the chunk, state n
+    const int wg = tid >> 7;        // compute warpgroup (kWG for the issuer warp)
+    const int odd = r & 1;
     const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
-    const int g = h / (a.H / a.G);
+    const int bg = b * a.G + h / (a.H / a.G);
     const int L = a.L;
     const size_t row0 = (static_cast<size_t>(b) * a.H + h) * kP;   // first channel row of this head in (B*D, L)
+    const size_t dt_row = (static_cast<size_t>(b) * a.H + h) * L;
 
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
-    uint64_t* mma_bar = tma_bar + 1;
+    uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    uint64_t* bar_bx = bar_c + 1;
+    uint64_t* mma_bar = bar_c + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
     float* s2s = reinterpret_cast<float*>(sm + kOffS2);
     float* wsv = reinterpret_cast<float*>(sm + kOffW);
     float* vsv = reinterpret_cast<float*>(sm + kOffV);
     float* wsum = reinterpret_cast<float*>(sm + kOffWarp);
 
-    if (tid == 0) {
-        mbar_init(tma_bar, 1);
+    auto issue_c = [&](int cc) {
+        mbar_arrive_expect_tx(bar_c, kCBytes);
+        tma_load_3d(sm + kOffC, &map_c, 0, cc * kQ, bg, bar_c);
+        tma_load_3d(sm + kOffC + 16384, &map_c, 64, cc * kQ, bg, bar_c);
+    };
+    auto issue_bx = [&](int cc) {
+        mbar_arrive_expect_tx(bar_bx, kBBytes + kXBytes);
+        tma_load_3d(sm + kOffBS, &map_b, 0, cc * kQ, bg, bar_bx);
+        tma_load_3d(sm + kOffBS + kBS, &map_b, 64, cc * kQ, bg, bar_bx);
+        tma_load_2d(sm + kOffX, &map_x, cc * kQ, static_cast<int>(row0), bar_bx);
+        tma_load_2d(sm + kOffX + 8192, &map_x, cc * kQ + 64, static_cast<int>(row0), bar_bx);
+    };
+
+    if (issuer) {
+        mbar_init(bar_c, 1);
+        mbar_init(bar_bx, 1);
         mbar_init(mma_bar, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_c);
         tma_prefetch_map(&map_b);
         tma_prefetch_map(&map_x);
+        tma_prefetch_map(&map_y);
+        issue_c(0);
+        issue_bx(0);
     }
     if (warp == 0) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
 
     const float A = a.A[h];
     const float A2 = A * kLog2e;
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.0f;
     const float dsk = a.Dskip ? a.Dskip[h] : 0.0f;
 
-    // the state, row n = tid of S (N x P)
-    float S[kP];
+    // compute threads: their part of the state, S[n = r][p] for the warpgroup's channels, and S^T (hi, lo)
+    float S[kPW];
+    if (!issuer_warp) {
 #pragma unroll
-    for (int p = 0; p < kP; ++p) S[p] = a.h0 ? a.h0[(row0 + p) * kN + tid] : 0.0f;
+        for (int q = 0; q < kPW; q += 2) {
+            const int p = wg * kPW + q;
+            S[q] = a.h0 ? a.h0[(row0 + p) * kN + r] : 0.0f;
+            S[q + 1] = a.h0 ? a.h0[(row0 + p + 1) * kN + r] : 0.0f;
+            float f, s;
+            pair_rows(S[q], S[q + 1], odd, f, s);
+            uint32_t hi, lo;
+            split_pair(f, s, hi, lo);
+            st_shared_u32(sm + kOffBS + swz(kBS, kRowStHi + p + odd, r & ~1), hi);
+            st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + p + odd, r & ~1), lo);
+        }
+    }
+    // warpgroup 0 reads each chunk's steps a chunk ahead
+    uint16_t dt_next = 0;   // raw bf16: converted when used, so that no instruction waits for the load early
+    if (wg == 0 && r < L) dt_next = reinterpret_cast<const uint16_t*>(a.dt)[dt_row + r];
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;   // this warp's TMEM lanes
 
-    const uint32_t sC = smem_u32(sm + kOffC), sB = smem_u32(sm + kOffB), sX = smem_u32(sm + kOffX);
+    const uint32_t sC = smem_u32(sm + kOffC), sBS = smem_u32(sm + kOffBS), sX = smem_u32(sm + kOffX);
+    const uint32_t sXs = smem_u32(sm + kOffXs), sXsLo = smem_u32(sm + kOffXsLo);
     const uint32_t sM = smem_u32(sm + kOffM), sMlo = smem_u32(sm + kOffMlo);
-    const uint32_t sBt = smem_u32(sm + kOffBt), sBtLo = smem_u32(sm + kOffBtLo);
-    const uint32_t sSt = smem_u32(sm + kOffSt), sStLo = smem_u32(sm + kOffStLo);
 
-    unsigned tma_phase = 0, mma_phase = 0;
-    bool tma_pending = false, mma_pending = false, ok = true;
+    unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
+    bool c_pend = true, bx_pend = true, mma_pend = false, ok = true;
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
-        // S^T (hi and lo) for this chunk's C S product; the previous chunk's MMAs that read it are complete
+        // step sizes and the cumulative decay of the chunk, by warpgroup 0 (steps past L: dt = 0, so a = 1
+        // and w = 0)
+        float inc = 0.0f;
+        if (wg == 0) {
+            const int t = t0 + r;
+            float dtv = 0.0f;
+            if (t < L) {
+                const float sr = bf16_to_f32(dt_next) + bias;
+                dtv = a.softplus ? softplus_fast(sr) : sr;
+            }
+            if (t + kQ < L) dt_next = reinterpret_cast<const uint16_t*>(a.dt)[dt_row + t + kQ];
+            inc = dtv * A2;
 #pragma unroll
-        for (int p = 0; p < kP; ++p) {
-            const uint16_t hi = f32_to_bf16(S[p]);
-            const uint32_t o = tc::sw128_offset(kP, p, tid);
-            *reinterpret_cast<uint16_t*>(sm + kOffSt + o) = hi;
-            *reinterpret_cast<uint16_t*>(sm + kOffStLo + o) = f32_to_bf16(S[p] - bf16_to_f32(hi));
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            if (lane == 31) wsum[warp] = inc;
+            wsv[r] = (a.zoh && A != 0.0f) ? expm1f(dtv * A) / A : dtv;
         }
-
-        if (tid == 0) {
-            mbar_arrive_expect_tx(tma_bar, kTileBytes);
-            const int bg = b * a.G + g;
-            tma_load_3d(sm + kOffC, &map_c, 0, t0, bg, tma_bar);
-            tma_load_3d(sm + kOffC + kQ * 128, &map_c, 64, t0, bg, tma_bar);
-            tma_load_3d(sm + kOffB, &map_b, 0, t0, bg, tma_bar);
-            tma_load_3d(sm + kOffB + kQ * 128, &map_b, 64, t0, bg, tma_bar);
-            tma_load_2d(sm + kOffX, &map_x, t0, static_cast<int>(row0), tma_bar);
-            tma_load_2d(sm + kOffX + kP * 128, &map_x, t0 + 64, static_cast<int>(row0), tma_bar);
-        }
-        tma_pending = true;
-
-        // step sizes and the cumulative decay of the chunk (steps past L: dt = 0, so a = 1 and w = 0)
-        const int t = t0 + tid;
-        float dtv = 0.0f;
-        if (t < L) {
-            const float sr = bf16_to_f32(reinterpret_cast<const uint16_t*>(a.dt)[(static_cast<size_t>(b) * a.H + h) * L + t]) + bias;
-            dtv = a.softplus ? softplus(sr) : sr;
-        }
-        float inc = dtv * A2;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += u;
-        }
-        if (lane == 31) wsum[warp] = inc;
         __syncthreads();
-        float s2 = inc;
-        for (int w2 = 0; w2 < warp; ++w2) s2 += wsum[w2];
-        float w = dtv;
-        if (a.zoh && A != 0.0f) w = expm1f(dtv * A) / A;
-        s2s[tid] = s2;
-        wsv[tid] = w;
+        if (wg == 0) {
+            for (int w2 = 0; w2 < warp; ++w2) inc += wsum[w2];
+            s2s[r] = inc;
+        }
         __syncthreads();
         const float s2_end = s2s[kQ - 1];
-        vsv[tid] = ex2(s2_end - s2) * w;
+        const float s2_row = s2s[r];
+        if (wg == 0) vsv[r] = ex2(s2_end - s2_row) * wsv[r];
 
-        // wait for C, B and X of this chunk
-        if (!wait_all(tma_bar, tma_phase)) {
+        // this chunk's C, B and X (issued a phase ahead)
+        if (!wait_all(bar_c, c_phase)) {
             ok = false;
             break;
         }
-        tma_phase ^= 1u;
-        tma_pending = false;
+        c_phase ^= 1u;
+        c_pend = false;
+        if (!wait_all(bar_bx, bx_phase)) {
+            ok = false;
+            break;
+        }
+        bx_phase ^= 1u;
+        bx_pend = false;
 
-        // G = C B^T and C S on the tensor cores
-        tc::fence_async_smem();   // S^T written by every thread
-        tc::fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
+            // [G | C S_hi | C S_lo] = C [B ; S^T hi ; S^T lo]^T: eight N = 256 products
             tc::fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t ko = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColG, tc::desc_k_sw128(sC + ko), tc::desc_k_sw128(sB + ko), tc::idesc_bf16(128, 128),
+                const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint32_t kb = (ks >> 2) * kBS + (ks & 3) * 32;
+                tc::mma_bf16(tmem + kColG, tc::desc_k_sw128(sC + ka), tc::desc_k_sw128(sBS + kb), tc::idesc_bf16(128, 256),
                              ks > 0);
             }
-#pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-                const int k = ks & 7;
-                const uint32_t ka = (k >> 2) * (kQ * 128) + (k & 3) * 32;
-                const uint32_t kb = (k >> 2) * (kP * 128) + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColY1, tc::desc_k_sw128(sC + ka), tc::desc_k_sw128((ks < 8 ? sSt : sStLo) + kb),
-                             tc::idesc_bf16(128, kP), ks > 0);
-            }
             tc::mma_commit(mma_bar);
-        }
-        mma_pending = true;
-
-        // meanwhile: row n = tid of the scaled B^T, (exp2(s_end - s_j) w_j B[j, n])_j, hi and lo
+            bulk_wait_read_all();   // the previous chunk's y store has left the M tile
+        } else if (!issuer_warp) {
+            // meanwhile: v o X (hi, lo) in 16-byte pieces of 8 steps, dealt over the compute threads
 #pragma unroll 1
-        for (int j0 = 0; j0 < kQ; j0 += 8) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = j0 + 2 * e;
-                const float v0 = vsv[j] * ld_bf16_shared(sm + kOffB + tc::sw128_offset(kQ, j, tid));
-                const float v1 = vsv[j + 1] * ld_bf16_shared(sm + kOffB + tc::sw128_offset(kQ, j + 1, tid));
-                split_pair(v0, v1, hi[e], lo[e]);
+            for (int idx = tid; idx < kP * (kQ / 8); idx += kCompute) {
+                const int p = idx >> 4, tc8 = (idx & 15) * 8;
+                const uint32_t o = swz(8192, p, tc8);
+                const uint4 xv = ld_shared_v4(sm + kOffX + o);
+                const float4 v0 = *reinterpret_cast<const float4*>(vsv + tc8);
+                const float4 v1 = *reinterpret_cast<const float4*>(vsv + tc8 + 4);
+                uint32_t hi[4], lo[4];
+                split_pair(bf16_lo(xv.x) * v0.x, bf16_hi(xv.x) * v0.y, hi[0], lo[0]);
+                split_pair(bf16_lo(xv.y) * v0.z, bf16_hi(xv.y) * v0.w, hi[1], lo[1]);
+                split_pair(bf16_lo(xv.z) * v1.x, bf16_hi(xv.z) * v1.y, hi[2], lo[2]);
+                split_pair(bf16_lo(xv.w) * v1.z, bf16_hi(xv.w) * v1.w, hi[3], lo[3]);
+                st_shared_v4(sm + kOffXs + o, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(sm + kOffXsLo + o, lo[0], lo[1], lo[2], lo[3]);
             }
-            const uint32_t o = tc::sw128_offset(kN, tid, j0);
-            st_shared_v4(sm + kOffBt + o, hi[0], hi[1], hi[2], hi[3]);
-            st_shared_v4(sm + kOffBtLo + o, lo[0], lo[1], lo[2], lo[3]);
+            tc::fence_async_smem();   // v o X, read by the increment issued after the next barrier
         }
-
+        mma_pend = true;
         if (!wait_all(mma_bar, mma_phase)) {
             ok = false;
             break;
         }
         mma_phase ^= 1u;
-        mma_pending = false;
+        mma_pend = false;
         tc::fence_after();
-
-        // row i = tid of M from row i of G (hi into M, lo into the B tile, which G no longer needs)
-#pragma unroll 1
-        for (int cb = 0; cb < kQ / 32; ++cb) {
-            float gv[32];
-            tc::tmem_ld32(tmem + tlane + kColG + cb * 32, gv);
+        if (issuer) {
+            if (c + 1 < nchunks) {   // C is free: the next chunk's copy overlaps the rest of this one
+                issue_c(c + 1);
+                c_pend = true;
+            }
+            // the increment B^T (v o X)^T (both terms of v o X), B read MN-major, under the M build
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = cb * 32 + q * 8 + 2 * e;
-                    const float v0 = j <= tid ? gv[q * 8 + 2 * e] * ex2(s2 - s2s[j]) * wsv[j] : 0.0f;
-                    const float v1 = j + 1 <= tid ? gv[q * 8 + 2 * e + 1] * ex2(s2 - s2s[j + 1]) * wsv[j + 1] : 0.0f;
-                    split_pair(v0, v1, hi[e], lo[e]);
-                }
-                const uint32_t o = tc::sw128_offset(kQ, tid, cb * 32 + q * 8);
-                st_shared_v4(sm + kOffM + o, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(sm + kOffMlo + o, lo[0], lo[1], lo[2], lo[3]);
+            for (int ks = 0; ks < 16; ++ks) {
+                const int k = ks & 7;
+                const uint32_t ka = sBS + k * 2048;   // 16 steps (rows t) of B per K step
+                const uint32_t kb = (ks < 8 ? sXs : sXsLo) + (k >> 2) * 8192 + (k & 3) * 32;
+                tc::mma_bf16(tmem + kColSc, tc::desc_mn_sw128(ka, kBS, 1024), tc::desc_k_sw128(kb),
+                             tc::idesc_bf16(128, kP, true), ks > 0);
             }
         }
-        tc::fence_async_smem();   // M and the scaled B^T
+
+        // row i = r of M from row i of G, in 16-column blocks dealt round-robin to the warpgroups; blocks
+        // wholly above the diagonal are zeros
+        if (!issuer_warp) {
+            const int quarter = warp & 3;
+            const f32x2 srow2 = pack2(s2_row, s2_row);
+#pragma unroll 1
+            for (int cb = 0; cb < kQ / 16; ++cb) {
+                if (cb % kWG != wg) continue;
+                const int jb = cb * 16;
+                float gv[16];
+                const bool live = 32 * quarter + 31 >= jb;   // warp-uniform: some row of this warp reaches jb
+                if (live) tc::tmem_ld16(tmem + tlane + kColG + jb, gv);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+                    const int j0 = jb + q * 8;
+                    if (live && j0 <= r) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j0 + 2 * e;
+                            const float2 sj = *reinterpret_cast<const float2*>(s2s + j);
+                            const float2 wj = *reinterpret_cast<const float2*>(wsv + j);
+                            const f32x2 ex = ex2x2(sub2(srow2, pack2(sj.x, sj.y)));
+                            const f32x2 m = mul2(mul2(pack2(gv[q * 8 + 2 * e], gv[q * 8 + 2 * e + 1]), ex),
+                                                 pack2(wj.x, wj.y));
+                            float v0, v1;
+                            unpack2(m, v0, v1);
+                            if (j0 + 8 > r) {   // the diagonal piece: mask above it, D skip on it
+                                v0 = j < r ? v0 : (j == r ? dsk + v0 : 0.0f);
+                                v1 = j + 1 < r ? v1 : (j + 1 == r ? dsk + v1 : 0.0f);
+                            }
+                            split_pair(v0, v1, hi[e], lo[e]);
+                        }
+                    }
+                    const uint32_t o = swz(16384, r, j0);
+                    st_shared_v4(sm + kOffM + o, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(sm + kOffMlo + o, lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        }
+        tc::fence_async_smem();   // M and v o X
         tc::fence_before();
         __syncthreads();
 
-        // M X and the state increment (scaled B^T) X on the tensor cores
-        if (tid == 0) {
+        if (issuer) {
+            // M X (both terms of M); the commit also covers the increment issued before it
             tc::fence_after();
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
                 const int k = ks & 7;
-                const uint32_t ka = (k >> 2) * (kQ * 128) + (k & 3) * 32;
-                const uint32_t kb = (k >> 2) * (kP * 128) + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColY2, tc::desc_k_sw128((ks < 8 ? sM : sMlo) + ka), tc::desc_k_sw128(sX + kb),
-                             tc::idesc_bf16(128, kP), ks > 0);
-            }
-#pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-                const int k = ks & 7;
-                const uint32_t ka = (k >> 2) * (kN * 128) + (k & 3) * 32;
-                const uint32_t kb = (k >> 2) * (kP * 128) + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColSc, tc::desc_k_sw128((ks < 8 ? sBt : sBtLo) + ka), tc::desc_k_sw128(sX + kb),
-                             tc::idesc_bf16(128, kP), ks > 0);
+                const uint32_t ka = (ks < 8 ? sM : sMlo) + (k >> 2) * 16384 + (k & 3) * 32;
+                const uint32_t kb = sX + (k >> 2) * 8192 + (k & 3) * 32;
+                tc::mma_bf16(tmem + kColY2, tc::desc_k_sw128(ka), tc::desc_k_sw128(kb), tc::idesc_bf16(128, kP), ks > 0);
             }
             tc::mma_commit(mma_bar);
         }
-        mma_pending = true;
+        mma_pend = true;
         if (!wait_all(mma_bar, mma_phase)) {
             ok = false;
             break;
         }
         mma_phase ^= 1u;
-        mma_pending = false;
+        mma_pend = false;
         tc::fence_after();
+        if (issuer && c + 1 < nchunks) {   // B and X are free
+            issue_bx(c + 1);
+            bx_pend = true;
+        }
 
-        // outputs of row i = tid (step t)
-        const float ei = ex2(s2);
+        if (!issuer_warp) {
+            // outputs of row i = r (step t), this warpgroup's channels, staged as the y tile in M's place
+            const int t = t0 + r;
+            const float ei = ex2(s2_row);
 #pragma unroll 1
-        for (int pc = 0; pc < kP / 32; ++pc) {
-            float y1[32], y2[32];
-            tc::tmem_ld32(tmem + tlane + kColY1 + pc * 32, y1);
-            tc::tmem_ld32(tmem + tlane + kColY2 + pc * 32, y2);
-            if (t < L) {
+            for (int pc = 0; pc < kPW / 16; ++pc) {
+                const int pb = wg * kPW + pc * 16;
+                float y1[16], y2[16];
+                tc::tmem_ld16(tmem + tlane + kColY1 + pb, y1);
+                tc::tmem_ld16(tmem + tlane + kColY1 + kP + pb, y2);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int p = pc * 32 + e;
-                    const size_t idx = (row0 + p) * L + t;
-                    const float xv = ld_bf16_shared(sm + kOffX + tc::sw128_offset(kP, p, tid));
-                    float yv = fmaf(ei, y1[e], y2[e]) + dsk * xv;
-                    if (a.z) yv *= silu(bf16_to_f32(reinterpret_cast<const uint16_t*>(a.z)[idx]));
-                    reinterpret_cast<uint16_t*>(a.y)[idx] = f32_to_bf16(yv);
+                for (int e = 0; e < 16; ++e) y1[e] += y2[e];
+                tc::tmem_ld16(tmem + tlane + kColY2 + pb, y2);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    y1[e] = fmaf(ei, y1[e], y2[e]);
+                    if (a.z && t < L)
+                        y1[e] *= silu(bf16_to_f32(reinterpret_cast<const uint16_t*>(a.z)[(row0 + pb + e) * L + t]));
+                }
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    float f, s;
+                    pair_rows(y1[e], y1[e + 1], odd, f, s);
+                    st_shared_u32(sm + kOffM + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s));
+                }
+            }
+            // the state: S <- exp2(s_end) S + increment (row n = r), and S^T (hi, lo) for the next chunk
+            const float eend = ex2(s2_end);
+#pragma unroll
+            for (int pc = 0; pc < kPW / 16; ++pc) {
+                const int pb = wg * kPW + pc * 16;
+                float sc[16];
+                tc::tmem_ld16(tmem + tlane + kColSc + pb, sc);
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const int q = pc * 16 + e;
+                    S[q] = fmaf(eend, S[q], sc[e]);
+                    S[q + 1] = fmaf(eend, S[q + 1], sc[e + 1]);
+                    float f, s;
+                    pair_rows(S[q], S[q + 1], odd, f, s);
+                    uint32_t hi, lo;
+                    split_pair(f, s, hi, lo);
+                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStHi + pb + e + odd, r & ~1), hi);
+                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + pb + e + odd, r & ~1), lo);
                 }
             }
         }
-        // the state: S <- exp2(s_end) S + increment (row n = tid)
-        const float eend = ex2(s2_end);
-#pragma unroll
-        for (int pc = 0; pc < kP / 32; ++pc) {
-            float sc[32];
-            tc::tmem_ld32(tmem + tlane + kColSc + pc * 32, sc);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) S[pc * 32 + e] = fmaf(eend, S[pc * 32 + e], sc[e]);
-        }
+        tc::fence_async_smem();   // the y tile and S^T
         tc::fence_before();
-        __syncthreads();   // every TMEM and shared read of this chunk is done before the next chunk's copies
+        __syncthreads();          // every TMEM and shared read of this chunk is done
+        if (issuer) {
+            tma_store_2d(&map_y, t0, static_cast<int>(row0), sm + kOffM);
+            if (t0 + 64 < L) tma_store_2d(&map_y, t0 + 64, static_cast<int>(row0), sm + kOffM + 8192);
+            bulk_commit_group();
+        }
     }
 
     if (ok) {
-        if (a.h_out) {
+        if (a.h_out && !issuer_warp) {
 #pragma unroll
-            for (int p = 0; p < kP; ++p) a.h_out[(row0 + p) * kN + tid] = S[p];
+            for (int q = 0; q < kPW; ++q) a.h_out[(row0 + wg * kPW + q) * kN + r] = S[q];
         }
-    } else {
-        // a wait gave up: record it, let this block's copies and MMAs still in flight finish (bounded)
-        if (tid == 0) {
-            atomicOr(&g_ssd_wait_error, 1u);
-            if (tma_pending) mbar_wait_bounded(tma_bar, tma_phase);
-            if (mma_pending) mbar_wait_bounded(mma_bar, mma_phase);
-        }
-        tc::fence_before();
-        __syncthreads();
+    } else if (issuer) {
+        // a wait gave up: record it and let this block's copies and products still in flight end (bounded)
+        atomicOr(&g_ssd_wait_error, 1u);
+        if (c_pend) mbar_wait_bounded(bar_c, c_phase);
+        if (bx_pend) mbar_wait_bounded(bar_bx, bx_phase);
+        if (mma_pend) mbar_wait_bounded(mma_bar, mma_phase);
     }
+    if (issuer) bulk_wait_all();   // the y stores are complete
+    tc::fence_before();
+    __syncthreads();
     if (warp == 0) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
@@ -355,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool ssd_tc_supported(int N, int P) { return N == kN && P == kP; }
 
 cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream) {
-    CUtensorMap mc, mb, mx;
+    CUtensorMap mc, mb, mx, my;
     const uint64_t bc_dims[3] = {static_cast<uint64_t>(kN), static_cast<uint64_t>(a.L),
                                  static_cast<uint64_t>(a.Bsz) * a.G};
     const uint64_t bc_strides[2] = {static_cast<uint64_t>(kN) * 2, static_cast<uint64_t>(a.L) * kN * 2};
@@ -365,11 +480,12 @@ cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream) {
     const uint32_t x_box[2] = {64, kP};
     if (!encode_bf16_map_sw128(&mc, a.Cm, 3, bc_dims, bc_strides, bc_box) ||
         !encode_bf16_map_sw128(&mb, a.Bm, 3, bc_dims, bc_strides, bc_box) ||
-        !encode_bf16_map_sw128(&mx, a.x, 2, x_dims, x_strides, x_box))
+        !encode_bf16_map_sw128(&mx, a.x, 2, x_dims, x_strides, x_box) ||
+        !encode_bf16_map_sw128(&my, a.y, 2, x_dims, x_strides, x_box))
         return cudaErrorInvalidValue;
     cudaError_t e = set_dynamic_smem_once(ssd_chunk_kernel, kSmemBytes);
     if (e != cudaSuccess) return e;
-    ssd_chunk_kernel<<<a.Bsz * a.H, kThreads, kSmemBytes, stream>>>(a, mc, mb, mx);
+    ssd_chunk_kernel<<<a.Bsz * a.H, kThreads, kSmemBytes, stream>>>(a, mc, mb, mx, my);
     return cudaGetLastError();
 }
 

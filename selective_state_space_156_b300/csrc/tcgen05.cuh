@@ -2,7 +2,7 @@
 // allocation, single-thread MMA issue with bf16 operands from shared memory and an fp32 accumulator in
 // TMEM, completion through an mbarrier, and the per-warp TMEM loads of an epilogue.
 //
-// Operand tiles are K-major in the 128-byte swizzle layout that a TMA copy with SWIZZLE_128B writes:
+// Operand tiles are in the 128-byte swizzle layout that a TMA copy with SWIZZLE_128B writes.  K-major:
 // rows of 64 bf16 (128 bytes), 8-row atoms of 1024 bytes in which the 16-byte chunk c of row r sits at
 // chunk c ^ (r % 8); a tile with K > 64 is a sequence of such 64-wide K blocks, each (rows x 128) bytes.
 // Tiles start on 1024-byte boundaries.  One MMA consumes K = 16 (32 bytes of every row); the k-th step
@@ -53,11 +53,25 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+// Shared-memory matrix descriptor of an MN-major, 128-byte-swizzled operand: lines of 64 M (or N)
+// elements (128 bytes), one per K index, 8-line atoms of 1024 bytes; `mn_stride` bytes between the
+// 64-element blocks along M (N), `k_stride` bytes between 8-line groups along K.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t mn_stride, uint32_t k_stride) {
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, shape M x N; B K-major, A K-major or
+// (a_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false) {
     return (1u << 4)                                   // D format: f32
            | (1u << 7)                                 // A format: bf16
            | (1u << 10)                                // B format: bf16
+           | (a_mn ? (1u << 15) : 0u)                  // A major-ness: MN
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
@@ -95,6 +109,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit columns of this thread's lane (as tmem_ld32)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // byte offset of element (row, k) in a K-major 128-byte-swizzled tile of `rows` rows
