@@ -602,8 +602,8 @@ ssm_status ssd_scan_fwd(const ssd_scan_params* p, ssm_stream_t stream) {
                     p->dstate);
     if (p->seqlen % 8 != 0)
         return fail(SSM_ERR_UNSUPPORTED, "%s: seqlen %d is not a multiple of 8", who, p->seqlen);
-    if (!aligned16(p->x) || !aligned16(p->Bm) || !aligned16(p->Cm) || !aligned16(p->y))
-        return fail(SSM_ERR_UNSUPPORTED, "%s: x, Bm, Cm and y must be 16-byte aligned", who);
+    if (!aligned16(p->x) || !aligned16(p->dt) || !aligned16(p->Bm) || !aligned16(p->Cm) || !aligned16(p->y))
+        return fail(SSM_ERR_UNSUPPORTED, "%s: x, dt, Bm, Cm and y must be 16-byte aligned", who);
     const size_t B = (size_t)p->batch, H = (size_t)p->nheads, L = (size_t)p->seqlen;
     const size_t D = H * (size_t)p->headdim, N = (size_t)p->dstate, G = (size_t)p->ngroups;
     if (B * H > 0x7fffffffu || B * D > 0x7fffffffu || B * G * L * N > ((size_t)1 << 40))

@@ -25,8 +25,8 @@
 // threads build M.  A dedicated warp issues the copies and the products; the
 // element-wise work is split over the compute warpgroups (each warp reads the TMEM lanes of its quarter
 // of the rows).  A chunk's C is fetched as soon as the previous chunk's first product is done, its B and
-// X as soon as the previous M X and increment are; dt is read a chunk ahead; y leaves through a TMA store
-// of the tile staged in M's place.
+// X (and dt) as soon as the previous M X and increment are; y leaves through a TMA store of the tile staged
+// in M's place.
 #include <cstdint>
 
 #include "bulk_copy.cuh"
@@ -66,7 +66,8 @@ constexpr int kOffS2 = kOffMlo + 2 * 16384;      // float s[Q]: cumulative log2 
 constexpr int kOffW = kOffS2 + kQ * 4;           // float w[Q]: input scale
 constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j) w_j
 constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
-constexpr int kOffBar = kOffWarp + 16;           // uint64 barriers: C landed, B and X landed, products done
+constexpr int kOffDt = kOffWarp + 16;            // bf16 dt[Q] of the chunk, copied with B and X
+constexpr int kOffBar = kOffDt + kQ * 2;         // uint64 barriers: C landed, B and X landed, products done
 constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;     // slack for aligning the base
@@ -82,6 +83,9 @@ __host__ __device__ constexpr uint32_t swz(int kb_stride, int row, int k) {
     return static_cast<uint32_t>((k >> 6) * kb_stride + row * 128 + ((((k >> 3) & 7) ^ (row & 7)) << 4) +
                                  ((k & 7) << 1));
 }
+
+// the compute threads alone (the issuer warp does not take part)
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kCompute) : "memory"); }
 
 // every thread waits; false on every thread if any of them gave up
 __device__ __forceinline__ bool wait_all(uint64_t* bar, unsigned parity) {
@@ -155,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm + kOffC + 16384, &map_c, 64, cc * kQ, bg, bar_c);
     };
     auto issue_bx = [&](int cc) {
-        mbar_arrive_expect_tx(bar_bx, kBBytes + kXBytes);
+        const unsigned dt_bytes = static_cast<unsigned>(min(kQ, L - cc * kQ)) * 2u;   // L % 8 == 0: whole 16 B
+        mbar_arrive_expect_tx(bar_bx, kBBytes + kXBytes + dt_bytes);
+        bulk_g2s(sm + kOffDt, reinterpret_cast<const uint16_t*>(a.dt) + dt_row + cc * kQ, dt_bytes, bar_bx);
         tma_load_3d(sm + kOffBS, &map_b, 0, cc * kQ, bg, bar_bx);
         tma_load_3d(sm + kOffBS + kBS, &map_b, 64, cc * kQ, bg, bar_bx);
         tma_load_2d(sm + kOffX, &map_x, cc * kQ, static_cast<int>(row0), bar_bx);
@@ -200,9 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + p + odd, r & ~1), lo);
         }
     }
-    // warpgroup 0 reads each chunk's steps a chunk ahead
-    uint16_t dt_next = 0;   // raw bf16: converted when used, so that no instruction waits for the load early
-    if (wg == 0 && r < L) dt_next = reinterpret_cast<const uint16_t*>(a.dt)[dt_row + r];
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
@@ -219,37 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
-        // step sizes and the cumulative decay of the chunk, by warpgroup 0 (steps past L: dt = 0, so a = 1
-        // and w = 0)
-        float inc = 0.0f;
-        if (wg == 0) {
-            const int t = t0 + r;
-            float dtv = 0.0f;
-            if (t < L) {
-                const float sr = bf16_to_f32(dt_next) + bias;
-                dtv = a.softplus ? softplus_fast(sr) : sr;
-            }
-            if (t + kQ < L) dt_next = reinterpret_cast<const uint16_t*>(a.dt)[dt_row + t + kQ];
-            inc = dtv * A2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += u;
-            }
-            if (lane == 31) wsum[warp] = inc;
-            wsv[r] = (a.zoh && A != 0.0f) ? expm1f(dtv * A) / A : dtv;
-        }
-        __syncthreads();
-        if (wg == 0) {
-            for (int w2 = 0; w2 < warp; ++w2) inc += wsum[w2];
-            s2s[r] = inc;
-        }
-        __syncthreads();
-        const float s2_end = s2s[kQ - 1];
-        const float s2_row = s2s[r];
-        if (wg == 0) vsv[r] = ex2(s2_end - s2_row) * wsv[r];
-
-        // this chunk's C, B and X (issued a phase ahead)
+        // this chunk's C, B, X and dt (issued a phase ahead)
         if (!wait_all(bar_c, c_phase)) {
             ok = false;
             break;
@@ -263,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bx_phase ^= 1u;
         bx_pend = false;
 
+        float s2_end = 0.0f, s2_row = 0.0f;
         if (issuer) {
             // [G | C S_hi | C S_lo] = C [B ; S^T hi ; S^T lo]^T: eight N = 256 products
             tc::fence_after();
@@ -276,7 +250,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(mma_bar);
             bulk_wait_read_all();   // the previous chunk's y store has left the M tile
         } else if (!issuer_warp) {
-            // meanwhile: v o X (hi, lo) in 16-byte pieces of 8 steps, dealt over the compute threads
+            // meanwhile: step sizes and the cumulative decay of the chunk, by warpgroup 0 (steps past L:
+            // dt = 0, so a = 1 and w = 0)
+            float inc = 0.0f;
+            if (wg == 0) {
+                float dtv = 0.0f;
+                if (t0 + r < L) {
+                    const float sr = bf16_to_f32(reinterpret_cast<const uint16_t*>(sm + kOffDt)[r]) + bias;
+                    dtv = a.softplus ? softplus_fast(sr) : sr;
+                }
+                inc = dtv * A2;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += u;
+                }
+                if (lane == 31) wsum[warp] = inc;
+                wsv[r] = (a.zoh && A != 0.0f) ? expm1f(dtv * A) / A : dtv;
+            }
+            compute_sync();
+            if (wg == 0) {
+                for (int w2 = 0; w2 < warp; ++w2) inc += wsum[w2];
+                s2s[r] = inc;
+            }
+            compute_sync();
+            s2_end = s2s[kQ - 1];
+            s2_row = s2s[r];
+            if (wg == 0) vsv[r] = ex2(s2_end - s2_row) * wsv[r];
+            compute_sync();
+            // v o X (hi, lo) in 16-byte pieces of 8 steps, dealt over the compute threads
 #pragma unroll 1
             for (int idx = tid; idx < kP * (kQ / 8); idx += kCompute) {
                 const int p = idx >> 4, tc8 = (idx & 15) * 8;
@@ -324,8 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int quarter = warp & 3;
             const f32x2 srow2 = pack2(s2_row, s2_row);
 #pragma unroll 1
-            for (int cb = 0; cb < kQ / 16; ++cb) {
-                if (cb % kWG != wg) continue;
+            for (int cb = wg; cb < kQ / 16; cb += kWG) {
                 const int jb = cb * 16;
                 float gv[16];
                 const bool live = 32 * quarter + 31 >= jb;   // warp-uniform: some row of this warp reaches jb
@@ -388,47 +389,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if (!issuer_warp) {
-            // outputs of row i = r (step t), this warpgroup's channels, staged as the y tile in M's place
+            // outputs of row i = r (step t) and the state row n = r, this warpgroup's channels: C S (both
+            // terms), M X and the increment read from TMEM together; y staged as the y tile in M's place,
+            // S <- exp2(s_end) S + increment and S^T (hi, lo) for the next chunk
             const int t = t0 + r;
             const float ei = ex2(s2_row);
-#pragma unroll 1
+            const float eend = ex2(s2_end);
+#pragma unroll
             for (int pc = 0; pc < kPW / 16; ++pc) {
                 const int pb = wg * kPW + pc * 16;
-                float y1[16], y2[16];
-                tc::tmem_ld16(tmem + tlane + kColY1 + pb, y1);
-                tc::tmem_ld16(tmem + tlane + kColY1 + kP + pb, y2);
+                float y1[16], v[2][16];
+                {
+                    const uint32_t ta[2] = {tmem + tlane + kColY1 + pb, tmem + tlane + kColY1 + kP + pb};
+                    tc::tmem_ld16xn<2>(ta, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) y1[e] += y2[e];
-                tc::tmem_ld16(tmem + tlane + kColY2 + pb, y2);
+                    for (int e = 0; e < 16; ++e) y1[e] = v[0][e] + v[1][e];
+                }
+                const uint32_t ta[2] = {tmem + tlane + kColY2 + pb, tmem + tlane + kColSc + pb};
+                tc::tmem_ld16xn<2>(ta, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    y1[e] = fmaf(ei, y1[e], y2[e]);
+                    y1[e] = fmaf(ei, y1[e], v[0][e]);
                     if (a.z && t < L)
                         y1[e] *= silu(bf16_to_f32(reinterpret_cast<const uint16_t*>(a.z)[(row0 + pb + e) * L + t]));
                 }
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
-                    float f, s;
-                    pair_rows(y1[e], y1[e + 1], odd, f, s);
-                    st_shared_u32(sm + kOffM + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s));
-                }
-            }
-            // the state: S <- exp2(s_end) S + increment (row n = r), and S^T (hi, lo) for the next chunk
-            const float eend = ex2(s2_end);
-#pragma unroll
-            for (int pc = 0; pc < kPW / 16; ++pc) {
-                const int pb = wg * kPW + pc * 16;
-                float sc[16];
-                tc::tmem_ld16(tmem + tlane + kColSc + pb, sc);
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
+                    float f, s2v;
+                    pair_rows(y1[e], y1[e + 1], odd, f, s2v);
+                    st_shared_u32(sm + kOffM + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s2v));
                     const int q = pc * 16 + e;
-                    S[q] = fmaf(eend, S[q], sc[e]);
-                    S[q + 1] = fmaf(eend, S[q + 1], sc[e + 1]);
-                    float f, s;
-                    pair_rows(S[q], S[q + 1], odd, f, s);
+                    S[q] = fmaf(eend, S[q], v[1][e]);
+                    S[q + 1] = fmaf(eend, S[q + 1], v[1][e + 1]);
+                    pair_rows(S[q], S[q + 1], odd, f, s2v);
                     uint32_t hi, lo;
-                    split_pair(f, s, hi, lo);
+                    split_pair(f, s2v, hi, lo);
                     st_shared_u32(sm + kOffBS + swz(kBS, kRowStHi + pb + e + odd, r & ~1), hi);
                     st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + pb + e + odd, r & ~1), lo);
                 }

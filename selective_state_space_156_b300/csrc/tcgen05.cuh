@@ -126,6 +126,49 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// n blocks of 16 consecutive columns of this thread's lane, at taddr[0..n), all waited for at once
+template <int kBlocks>
+__device__ __forceinline__ void tmem_ld16xn(const uint32_t (&taddr)[kBlocks], float (&v)[kBlocks][16]) {
+    static_assert(kBlocks == 2 || kBlocks == 4, "blocks");
+    uint32_t r[kBlocks][16];
+#define SSM_TC_LD16(i)                                                                                          \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, " \
+                 "%13, %14, %15}, [%16];"                                                                       \
+                 : "=r"(r[i][0]), "=r"(r[i][1]), "=r"(r[i][2]), "=r"(r[i][3]), "=r"(r[i][4]), "=r"(r[i][5]),      \
+                   "=r"(r[i][6]), "=r"(r[i][7]), "=r"(r[i][8]), "=r"(r[i][9]), "=r"(r[i][10]), "=r"(r[i][11]),   \
+                   "=r"(r[i][12]), "=r"(r[i][13]), "=r"(r[i][14]), "=r"(r[i][15])                               \
+                 : "r"(taddr[i])                                                                                \
+                 : "memory")
+    SSM_TC_LD16(0);
+    SSM_TC_LD16(1);
+    if constexpr (kBlocks == 4) {
+        SSM_TC_LD16(2);
+        SSM_TC_LD16(3);
+    }
+#undef SSM_TC_LD16
+    // the registers are written asynchronously: this wait, in a statement that lists them all as in-out
+    // operands, keeps every use of them behind it
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]),
+                 "+r"(r[0][4]), "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]),
+                 "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]), "+r"(r[0][15])
+                 :: "memory");
+    asm volatile("" : "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]), "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]),
+                 "+r"(r[1][6]), "+r"(r[1][7]), "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]),
+                 "+r"(r[1][12]), "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]) :: "memory");
+    if constexpr (kBlocks == 4) {
+        asm volatile("" : "+r"(r[2][0]), "+r"(r[2][1]), "+r"(r[2][2]), "+r"(r[2][3]), "+r"(r[2][4]), "+r"(r[2][5]),
+                     "+r"(r[2][6]), "+r"(r[2][7]), "+r"(r[2][8]), "+r"(r[2][9]), "+r"(r[2][10]), "+r"(r[2][11]),
+                     "+r"(r[2][12]), "+r"(r[2][13]), "+r"(r[2][14]), "+r"(r[2][15]) :: "memory");
+        asm volatile("" : "+r"(r[3][0]), "+r"(r[3][1]), "+r"(r[3][2]), "+r"(r[3][3]), "+r"(r[3][4]), "+r"(r[3][5]),
+                     "+r"(r[3][6]), "+r"(r[3][7]), "+r"(r[3][8]), "+r"(r[3][9]), "+r"(r[3][10]), "+r"(r[3][11]),
+                     "+r"(r[3][12]), "+r"(r[3][13]), "+r"(r[3][14]), "+r"(r[3][15]) :: "memory");
+    }
+#pragma unroll
+    for (int b = 0; b < kBlocks; ++b)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[b][i] = __uint_as_float(r[b][i]);
+}
+
 // byte offset of element (row, k) in a K-major 128-byte-swizzled tile of `rows` rows
 __host__ __device__ constexpr uint32_t sw128_offset(int rows, int row, int k) {
     return static_cast<uint32_t>((k >> 6) * rows * 128 + row * 128 + ((((k >> 3) & 7) ^ (row & 7)) << 4) +
