@@ -68,7 +68,7 @@ constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j
 constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
 constexpr int kOffDt = kOffWarp + 16;            // bf16 dt[Q] of the chunk, copied with B and X
 constexpr int kOffBar = kOffDt + kQ * 2;         // uint64 barriers: C landed, B and X landed, products done
-constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base
+constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base, int abort flag
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;     // slack for aligning the base
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -87,10 +87,22 @@ __host__ __device__ constexpr uint32_t swz(int kb_stride, int row, int k) {
 // the compute threads alone (the issuer warp does not take part)
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kCompute) : "memory"); }
 
-// every thread waits; false on every thread if any of them gave up
-__device__ __forceinline__ bool wait_all(uint64_t* bar, unsigned parity) {
-    const bool ok = mbar_wait_bounded(bar, parity);
-    return __syncthreads_or(!ok) == 0;
+// This thread waits for the phase; false when it gave up (about one second) or some thread of the block
+// already had, in which case it raises, or finds, the block's abort flag.  After an abort the block runs
+// its loop to the end without waiting or issuing anything, so that every thread still meets every
+// barrier, and reports the failure.
+__device__ __forceinline__ bool wait_own(uint64_t* bar, unsigned parity, volatile int* abort_flag) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
 }
 
 __device__ __forceinline__ void st_shared_v4(unsigned char* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -148,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar_bx = bar_c + 1;
     uint64_t* mma_bar = bar_c + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffTmem + 4);
     float* s2s = reinterpret_cast<float*>(sm + kOffS2);
     float* wsv = reinterpret_cast<float*>(sm + kOffW);
     float* vsv = reinterpret_cast<float*>(sm + kOffV);
@@ -169,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (issuer) {
+        *abort_flag = 0;
         mbar_init(bar_c, 1);
         mbar_init(bar_bx, 1);
         mbar_init(mma_bar, 1);
@@ -218,26 +232,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sM = smem_u32(sm + kOffM), sMlo = smem_u32(sm + kOffMlo);
 
     unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
-    bool c_pend = true, bx_pend = true, mma_pend = false, ok = true;
+    // the issuer's view of its asynchronous work: issued and not yet seen complete by its own wait, with
+    // the parity of the phase that completes it (a chunk's copies: the chunk's; products: their order)
+    bool c_pend = true, bx_pend = true, mma_pend = false;
+    unsigned c_par = 0, bx_par = 0, mma_par = 0;
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
-        // this chunk's C, B, X and dt (issued a phase ahead)
-        if (!wait_all(bar_c, c_phase)) {
-            ok = false;
-            break;
-        }
+        // this chunk's C, B, X and dt (issued a phase ahead); each thread waits for itself
+        if (wait_own(bar_c, c_phase, abort_flag)) c_pend = false;
+        if (wait_own(bar_bx, bx_phase, abort_flag)) bx_pend = false;
         c_phase ^= 1u;
-        c_pend = false;
-        if (!wait_all(bar_bx, bx_phase)) {
-            ok = false;
-            break;
-        }
         bx_phase ^= 1u;
-        bx_pend = false;
 
         float s2_end = 0.0f, s2_row = 0.0f;
-        if (issuer) {
+        if (issuer && !*abort_flag) {
             // [G | C S_hi | C S_lo] = C [B ; S^T hi ; S^T lo]^T: eight N = 256 products
             tc::fence_after();
 #pragma unroll
@@ -248,6 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ks > 0);
             }
             tc::mma_commit(mma_bar);
+            mma_pend = true;
+            mma_par = 0;   // the first of the chunk's two commits
+        }
+        if (issuer) {
             bulk_wait_read_all();   // the previous chunk's y store has left the M tile
         } else if (!issuer_warp) {
             // meanwhile: step sizes and the cumulative decay of the chunk, by warpgroup 0 (steps past L:
@@ -296,18 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_async_smem();   // v o X, read by the increment issued after the next barrier
         }
-        mma_pend = true;
-        if (!wait_all(mma_bar, mma_phase)) {
-            ok = false;
-            break;
-        }
+        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) mma_pend = false;
         mma_phase ^= 1u;
-        mma_pend = false;
+        tc::fence_before();
+        __syncthreads();   // v o X is complete (and G is read by the M build behind this)
         tc::fence_after();
-        if (issuer) {
+        if (issuer && !*abort_flag) {
             if (c + 1 < nchunks) {   // C is free: the next chunk's copy overlaps the rest of this one
                 issue_c(c + 1);
                 c_pend = true;
+                c_par = (c + 1) & 1;
             }
             // the increment B^T (v o X)^T (both terms of v o X), B read MN-major, under the M build
 #pragma unroll
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before();
         __syncthreads();
 
-        if (issuer) {
+        if (issuer && !*abort_flag) {
             // M X (both terms of M); the commit also covers the increment issued before it
             tc::fence_after();
 #pragma unroll
@@ -374,18 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_bf16(tmem + kColY2, tc::desc_k_sw128(ka), tc::desc_k_sw128(kb), tc::idesc_bf16(128, kP), ks > 0);
             }
             tc::mma_commit(mma_bar);
+            mma_pend = true;
+            mma_par = 1;   // the second
         }
-        mma_pend = true;
-        if (!wait_all(mma_bar, mma_phase)) {
-            ok = false;
-            break;
-        }
+        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) mma_pend = false;
         mma_phase ^= 1u;
-        mma_pend = false;
         tc::fence_after();
-        if (issuer && c + 1 < nchunks) {   // B and X are free
+        if (issuer && c + 1 < nchunks && !*abort_flag) {   // B and X are free
             issue_bx(c + 1);
             bx_pend = true;
+            bx_par = (c + 1) & 1;
         }
 
         if (!issuer_warp) {
@@ -432,24 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_async_smem();   // the y tile and S^T
         tc::fence_before();
         __syncthreads();          // every TMEM and shared read of this chunk is done
-        if (issuer) {
+        if (issuer && !*abort_flag) {
             tma_store_2d(&map_y, t0, static_cast<int>(row0), sm + kOffM);
             if (t0 + 64 < L) tma_store_2d(&map_y, t0 + 64, static_cast<int>(row0), sm + kOffM + 8192);
             bulk_commit_group();
         }
     }
 
+    const bool ok = *abort_flag == 0;   // read after the loop's last barrier: the same on every thread
     if (ok) {
         if (a.h_out && !issuer_warp) {
 #pragma unroll
             for (int q = 0; q < kPW; ++q) a.h_out[(row0 + wg * kPW + q) * kN + r] = S[q];
         }
     } else if (issuer) {
-        // a wait gave up: record it and let this block's copies and products still in flight end (bounded)
+        // a wait gave up: record it and let this block's copies and products still in flight end (bounded;
+        // products complete in order, so the last commit covers every earlier one)
         atomicOr(&g_ssd_wait_error, 1u);
-        if (c_pend) mbar_wait_bounded(bar_c, c_phase);
-        if (bx_pend) mbar_wait_bounded(bar_bx, bx_phase);
-        if (mma_pend) mbar_wait_bounded(mma_bar, mma_phase);
+        if (c_pend) mbar_wait_bounded(bar_c, c_par);
+        if (bx_pend) mbar_wait_bounded(bar_bx, bx_par);
+        if (mma_pend) mbar_wait_bounded(mma_bar, mma_par);
     }
     if (issuer) bulk_wait_all();   // the y stores are complete
     tc::fence_before();
