@@ -24,7 +24,8 @@
 // the state increment in 320..383; the increment is issued as soon as v o X is built and runs while the
 // threads build M.  A dedicated warp issues the copies and the products; the
 // element-wise work is split over the compute warpgroups (each warp reads the TMEM lanes of its quarter
-// of the rows).  A chunk's C is fetched as soon as the previous chunk's first product is done, its B and
+// of the rows).  The increment completes on a barrier of its own, so that the state update runs while
+// M X is still on the tensor cores.  A chunk's C is fetched as soon as the previous chunk's first product is done, its B and
 // X (and dt) as soon as the previous M X and increment are; y leaves through a TMA store of the tile staged
 // in M's place.
 #include <cstdint>
@@ -67,7 +68,8 @@ constexpr int kOffW = kOffS2 + kQ * 4;           // float w[Q]: input scale
 constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j) w_j
 constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
 constexpr int kOffDt = kOffWarp + 16;            // bf16 dt[Q] of the chunk, copied with B and X
-constexpr int kOffBar = kOffDt + kQ * 2;         // uint64 barriers: C landed, B and X landed, products done
+constexpr int kOffBar = kOffDt + kQ * 2;         // uint64 barriers: C landed, B and X landed, products
+                                                 //   done, increment done
 constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base, int abort flag
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;     // slack for aligning the base
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + kOffBar);
     uint64_t* bar_bx = bar_c + 1;
     uint64_t* mma_bar = bar_c + 2;
+    uint64_t* inc_bar = bar_c + 3;   // the chunk's state increment is done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffTmem + 4);
     float* s2s = reinterpret_cast<float*>(sm + kOffS2);
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_c, 1);
         mbar_init(bar_bx, 1);
         mbar_init(mma_bar, 1);
+        mbar_init(inc_bar, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_c);
         tma_prefetch_map(&map_b);
@@ -234,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
     // the issuer's view of its asynchronous work: issued and not yet seen complete by its own wait, with
     // the parity of the phase that completes it (a chunk's copies: the chunk's; products: their order)
-    bool c_pend = true, bx_pend = true, mma_pend = false;
-    unsigned c_par = 0, bx_par = 0, mma_par = 0;
+    bool c_pend = true, bx_pend = true, mma_pend = false, inc_pend = false;
+    unsigned c_par = 0, bx_par = 0, mma_par = 0, inc_par = 0;
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
@@ -329,6 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_bf16(tmem + kColSc, tc::desc_mn_sw128(ka, kBS, 1024), tc::desc_k_sw128(kb),
                              tc::idesc_bf16(128, kP, true), ks > 0);
             }
+            tc::mma_commit(inc_bar);
+            inc_pend = true;
+            inc_par = c & 1;
         }
 
         // row i = r of M from row i of G, in 16-column blocks dealt round-robin to the warpgroups; blocks
@@ -388,6 +395,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_pend = true;
             mma_par = 1;   // the second
         }
+        // the state first, while M X runs: S <- exp2(s_end) S + increment (row n = r), S^T (hi, lo) for the
+        // next chunk
+        if (wait_own(inc_bar, c & 1, abort_flag) && issuer) inc_pend = false;
+        tc::fence_after();
+        if (!issuer_warp) {
+            const float eend = ex2(s2_end);
+#pragma unroll
+            for (int pc = 0; pc < kPW / 16; ++pc) {
+                const int pb = wg * kPW + pc * 16;
+                float sc[16];
+                tc::tmem_ld16(tmem + tlane + kColSc + pb, sc);
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const int q = pc * 16 + e;
+                    S[q] = fmaf(eend, S[q], sc[e]);
+                    S[q + 1] = fmaf(eend, S[q + 1], sc[e + 1]);
+                    float f, s2v;
+                    pair_rows(S[q], S[q + 1], odd, f, s2v);
+                    uint32_t hi, lo;
+                    split_pair(f, s2v, hi, lo);
+                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStHi + pb + e + odd, r & ~1), hi);
+                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + pb + e + odd, r & ~1), lo);
+                }
+            }
+        }
         if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) mma_pend = false;
         mma_phase ^= 1u;
         tc::fence_after();
@@ -398,12 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if (!issuer_warp) {
-            // outputs of row i = r (step t) and the state row n = r, this warpgroup's channels: C S (both
-            // terms), M X and the increment read from TMEM together; y staged as the y tile in M's place,
-            // S <- exp2(s_end) S + increment and S^T (hi, lo) for the next chunk
+            // outputs of row i = r (step t), this warpgroup's channels: C S (both terms) and M X from TMEM,
+            // y staged as the y tile in M's place
             const int t = t0 + r;
             const float ei = ex2(s2_row);
-            const float eend = ex2(s2_end);
 #pragma unroll
             for (int pc = 0; pc < kPW / 16; ++pc) {
                 const int pb = wg * kPW + pc * 16;
@@ -414,8 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) y1[e] = v[0][e] + v[1][e];
                 }
-                const uint32_t ta[2] = {tmem + tlane + kColY2 + pb, tmem + tlane + kColSc + pb};
-                tc::tmem_ld16xn<2>(ta, v);
+                tc::tmem_ld16(tmem + tlane + kColY2 + pb, v[0]);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     y1[e] = fmaf(ei, y1[e], v[0][e]);
@@ -427,14 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float f, s2v;
                     pair_rows(y1[e], y1[e + 1], odd, f, s2v);
                     st_shared_u32(sm + kOffM + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s2v));
-                    const int q = pc * 16 + e;
-                    S[q] = fmaf(eend, S[q], v[1][e]);
-                    S[q + 1] = fmaf(eend, S[q + 1], v[1][e + 1]);
-                    pair_rows(S[q], S[q + 1], odd, f, s2v);
-                    uint32_t hi, lo;
-                    split_pair(f, s2v, hi, lo);
-                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStHi + pb + e + odd, r & ~1), hi);
-                    st_shared_u32(sm + kOffBS + swz(kBS, kRowStLo + pb + e + odd, r & ~1), lo);
                 }
             }
         }
@@ -460,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicOr(&g_ssd_wait_error, 1u);
         if (c_pend) mbar_wait_bounded(bar_c, c_par);
         if (bx_pend) mbar_wait_bounded(bar_bx, bx_par);
+        if (inc_pend) mbar_wait_bounded(inc_bar, inc_par);
         if (mma_pend) mbar_wait_bounded(mma_bar, mma_par);
     }
     if (issuer) bulk_wait_all();   // the y stores are complete
