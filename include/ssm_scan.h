@@ -340,7 +340,7 @@ SSM_API ssm_status ssm_state_update_conv(const ssm_step_params *p, ssm_stream_t 
  *   Dskip, dt_bias (H)    float32 or NULL
  *   h0, h_out (B, H, P, N) float32 initial state (NULL: zeros) and final state (NULL: not wanted);
  *                                 h0 may be the same buffer as h_out
- * Supported: headdim P = 64, dstate N = 128, ngroups dividing nheads, seqlen % 8 == 0 (the rows of x,
+ * Supported: headdim P = 64, dstate N = 64 or 128, ngroups dividing nheads, seqlen % 8 == 0 (the rows of x,
  * dt and y are moved by TMA bulk copies, whose rows are whole multiples of 16 bytes), x, dt, Bm, Cm
  * and y 16-byte aligned.  y must not overlap any input; h_out must not overlap y or any input but h0.
  * Errors: SSM_ERR_INVALID_ARG (null params or required pointer, size <= 0, bad flag, overlap),

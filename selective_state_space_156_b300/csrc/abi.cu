@@ -598,7 +598,7 @@ ssm_status ssd_scan_fwd(const ssd_scan_params* p, ssm_stream_t stream) {
     if (p->nheads % p->ngroups != 0)
         return fail(SSM_ERR_INVALID_ARG, "%s: ngroups %d does not divide nheads %d", who, p->ngroups, p->nheads);
     if (!ssm::ssd_tc_supported(p->dstate, p->headdim))
-        return fail(SSM_ERR_UNSUPPORTED, "%s: headdim %d / dstate %d not supported (64 / 128)", who, p->headdim,
+        return fail(SSM_ERR_UNSUPPORTED, "%s: headdim %d / dstate %d not supported (64 / 64 or 128)", who, p->headdim,
                     p->dstate);
     if (p->seqlen % 8 != 0)
         return fail(SSM_ERR_UNSUPPORTED, "%s: seqlen %d is not a multiple of 8", who, p->seqlen);
@@ -625,7 +625,7 @@ ssm_status ssd_scan_fwd(const ssd_scan_params* p, ssm_stream_t stream) {
         if (p->h0 && p->h0 != p->h_out && overlaps(p->h_out, hb, p->h0, hb))
             return fail(SSM_ERR_INVALID_ARG, "%s: h_out partly overlaps h0", who);
     }
-    ssm::SsdArgs a{p->batch, p->nheads, p->ngroups, p->seqlen, p->x, p->dt, p->A, p->Bm, p->Cm, p->Dskip,
+    ssm::SsdArgs a{p->batch, p->nheads, p->ngroups, p->seqlen, p->dstate, p->x, p->dt, p->A, p->Bm, p->Cm, p->Dskip,
                    p->dt_bias, p->z, p->h0, p->h_out, p->y, p->delta_softplus, p->zoh};
     cudaError_t e = ssm::launch_ssd_chunked(a, (cudaStream_t)stream);
     if (e == cudaErrorInvalidValue) return fail(SSM_ERR_UNSUPPORTED, "%s: tensor map encoding refused the layout", who);

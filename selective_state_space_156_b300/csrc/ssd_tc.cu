@@ -41,7 +41,7 @@ namespace ssm {
 namespace {
 
 constexpr int kQ = 128;   // chunk length
-constexpr int kN = 128;   // state size
+constexpr int kN = 128;   // state size of the tiles; a problem with N = 64 leaves states 64..127 zero
 constexpr int kP = 64;    // channels per head
 #ifndef SSD_COMPUTE_WARPGROUPS
 #define SSD_COMPUTE_WARPGROUPS 4
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < kPW; q += 2) {
             const int p = wg * kPW + q;
-            S[q] = a.h0 ? a.h0[(row0 + p) * kN + r] : 0.0f;
-            S[q + 1] = a.h0 ? a.h0[(row0 + p + 1) * kN + r] : 0.0f;
+            S[q] = (a.h0 && r < a.N) ? a.h0[(row0 + p) * a.N + r] : 0.0f;
+            S[q + 1] = (a.h0 && r < a.N) ? a.h0[(row0 + p + 1) * a.N + r] : 0.0f;
             float f, s;
             pair_rows(S[q], S[q + 1], odd, f, s);
             uint32_t hi, lo;
@@ -473,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
         if (a.h_out && !issuer_warp) {
 #pragma unroll
-            for (int q = 0; q < kPW; ++q) a.h_out[(row0 + wg * kPW + q) * kN + r] = S[q];
+            for (int q = 0; q < kPW; ++q)
+                if (r < a.N) a.h_out[(row0 + wg * kPW + q) * a.N + r] = S[q];
         }
     } else if (issuer) {
         // a wait gave up: record it and let this block's copies and products still in flight end (bounded;
@@ -495,13 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool ssd_tc_supported(int N, int P) { return N == kN && P == kP; }
+// N = 64 runs the same tiles: the B and C maps end at state 64, so the copies fill states 64..127 with
+// zeros, which leave G, C S and the increment exact and those rows of S at zero.
+bool ssd_tc_supported(int N, int P) { return (N == kN || N == 64) && P == kP; }
 
 cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream) {
     CUtensorMap mc, mb, mx, my;
-    const uint64_t bc_dims[3] = {static_cast<uint64_t>(kN), static_cast<uint64_t>(a.L),
+    const uint64_t bc_dims[3] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.L),
                                  static_cast<uint64_t>(a.Bsz) * a.G};
-    const uint64_t bc_strides[2] = {static_cast<uint64_t>(kN) * 2, static_cast<uint64_t>(a.L) * kN * 2};
+    const uint64_t bc_strides[2] = {static_cast<uint64_t>(a.N) * 2, static_cast<uint64_t>(a.L) * a.N * 2};
     const uint32_t bc_box[3] = {64, kQ, 1};
     const uint64_t x_dims[2] = {static_cast<uint64_t>(a.L), static_cast<uint64_t>(a.Bsz) * a.H * kP};
     const uint64_t x_strides[1] = {static_cast<uint64_t>(a.L) * 2};

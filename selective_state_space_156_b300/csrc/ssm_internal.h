@@ -135,17 +135,17 @@ cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* 
 
 // The Mamba-2 (SSD) chunked scan on the tensor cores (ssd_tc.cu), after host-side validation.
 struct SsdArgs {
-    int Bsz, H, G, L;          // batch, heads, groups, steps; head dim 64 and state 128 (ssd_tc_supported)
+    int Bsz, H, G, L, N;       // batch, heads, groups, steps, state (64 or 128); head dim 64 (ssd_tc_supported)
     const void* x;             // (B, H*64, L) bf16
     const void* dt;            // (B, H, L) bf16
     const float* A;            // (H)
-    const void* Bm;            // (B, G, L, 128) bf16
-    const void* Cm;            // (B, G, L, 128) bf16
+    const void* Bm;            // (B, G, L, N) bf16
+    const void* Cm;            // (B, G, L, N) bf16
     const float* Dskip;        // (H) or NULL
     const float* dt_bias;      // (H) or NULL
     const void* z;             // (B, H*64, L) bf16 or NULL
-    const float* h0;           // (B, H, 64, 128) or NULL
-    float* h_out;              // (B, H, 64, 128) or NULL
+    const float* h0;           // (B, H, 64, N) or NULL
+    float* h_out;              // (B, H, 64, N) or NULL
     void* y;                   // (B, H*64, L) bf16
     int softplus, zoh;
 };

@@ -255,7 +255,7 @@ def _ssd_params():
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("headdim", 32, ssm.SSM_ERR_UNSUPPORTED), ("dstate", 64, ssm.SSM_ERR_UNSUPPORTED),
+    ("headdim", 32, ssm.SSM_ERR_UNSUPPORTED), ("dstate", 32, ssm.SSM_ERR_UNSUPPORTED),
     ("seqlen", 100, ssm.SSM_ERR_UNSUPPORTED), ("ngroups", 3, ssm.SSM_ERR_INVALID_ARG),
     ("batch", 0, ssm.SSM_ERR_INVALID_ARG), ("seqlen", -8, ssm.SSM_ERR_INVALID_ARG),
     ("zoh", 2, ssm.SSM_ERR_INVALID_ARG), ("x", None, ssm.SSM_ERR_INVALID_ARG), ("dt", None, ssm.SSM_ERR_INVALID_ARG),

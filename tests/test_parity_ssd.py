@@ -2,7 +2,8 @@
 the C ABI.
 
 Small problems cover the flags (softplus on or off, zero-order hold or the simplified input scale, gate,
-initial state), one to four groups, a ragged last chunk, the shortest accepted sequence and an A = 0 head;
+initial state), one to four groups, a ragged last chunk, the shortest accepted sequence, d_state 64 and
+an A = 0 head;
 the Mamba-2 2.7B layer (8 x 80 heads x 64 x 128 states x 2048 steps) is checked on sampled channels.
 Tolerances: y (bf16) |err| <= 2e-2 (|y_ref| + rms(y_ref)) per element and, across all elements,
 rms(err) <= 5e-3 rms(y_ref); the final state (fp32) |err| <= 1e-3 (1 + |h_ref|)."""
@@ -38,9 +39,9 @@ def _check_y(y, ref, what):
     assert agg <= 5e-3 * rms, f"{what}: rms error {agg:.3e} above 5e-3 of rms(y) {rms:.3e}"
 
 
-def _small(L, G, seed, *, z=True, h0=True, zoh=False, softplus=True, H=4, Bsz=2):
+def _small(L, G, seed, *, z=True, h0=True, zoh=False, softplus=True, H=4, Bsz=2, N=128):
     d = workloads.make_ssd_inputs(workloads.SSD_CONFIGS["ssd_small"], batch=Bsz, nheads=H, ngroups=G, seqlen=L,
-                                  with_h0=h0, has_z=z, seed=seed)
+                                  dstate=N, with_h0=h0, has_z=z, seed=seed)
     d["zoh"] = zoh
     d["delta_softplus"] = softplus
     if not softplus:  # dt = raw + bias directly: a positive step
@@ -69,6 +70,17 @@ def test_ssd_groups(G):
     ref_y, ref_h, _ = ssd_scan(d)
     _check_y(y, ref_y.reshape(y.shape), f"y G={G}")
     assert_close(h, ref_h.reshape(h.shape), h_tolerance(ref_h.reshape(h.shape), torch.bfloat16), "h_out")
+
+
+@pytest.mark.parametrize("L,flags", [(200, 0), (384, 1), (8, 2), (136, 3)])
+def test_ssd_state_64(L, flags):
+    """d_state 64: the same kernel with the B and C copies ending at state 64 (states 64..127 read as zeros)."""
+    d = _small(L, 2, 3500 + L + flags, N=64, **FLAGS[flags])
+    y, h = _run(d)
+    assert tuple(h.shape) == (2, 4, 64, 64)
+    ref_y, ref_h, _ = ssd_scan(d)
+    _check_y(y, ref_y.reshape(y.shape), f"y N=64 L={L}")
+    assert_close(h, ref_h.reshape(h.shape), h_tolerance(ref_h.reshape(h.shape), torch.bfloat16), "h_out N=64")
 
 
 @pytest.mark.parametrize("zoh", [False, True])

@@ -227,8 +227,8 @@ SSD_CONFIGS = {
 
 
 def make_ssd_inputs(cfg: SsdConfig, *, batch: Optional[int] = None, nheads: Optional[int] = None,
-                    ngroups: Optional[int] = None, seqlen: Optional[int] = None, with_h0: bool = False,
-                    has_z: Optional[bool] = None, seed: Optional[int] = None) -> dict:
+                    ngroups: Optional[int] = None, seqlen: Optional[int] = None, dstate: Optional[int] = None,
+                    with_h0: bool = False, has_z: Optional[bool] = None, seed: Optional[int] = None) -> dict:
     """CPU tensors for one SSD workload (bf16 x, dt, B, C, z; fp32 A, D skip, dt bias, h0).
 
       x, z   (B, H * P, L)   channel d = h * P + p, contiguous in L (the Mamba-1 layout)
@@ -242,7 +242,8 @@ def make_ssd_inputs(cfg: SsdConfig, *, batch: Optional[int] = None, nheads: Opti
     H = cfg.nheads if nheads is None else nheads
     G = cfg.ngroups if ngroups is None else ngroups
     L = cfg.seqlen if seqlen is None else seqlen
-    P, N = cfg.headdim, cfg.dstate
+    P = cfg.headdim
+    N = cfg.dstate if dstate is None else dstate
     base = cfg.seed if seed is None else seed
     bf = torch.bfloat16
 
