@@ -85,7 +85,7 @@ def scan_fp32_ops(cfg) -> int:
 # workload, from the ncu capture summarised under profiles/, keyed by the hash of the kernel sources it
 # was taken on: after any change to those sources the figure no longer applies and is reported as null.
 KERNEL_SOURCES = ("scan_p16.cuh", "ssm_device.cuh", "ssm_internal.h", "abi.cu")
-TRAFFIC = {"mamba1.4b_conv": (405753600 + 115468800, "3491736db9ed6480")}
+TRAFFIC = {"mamba1.4b_conv": (405689344 + 114424832, "6ed0b83f00927460")}
 
 
 def kernel_source_hash() -> str:
