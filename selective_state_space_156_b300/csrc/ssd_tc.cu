@@ -21,13 +21,13 @@
 // product per K step.
 //
 // Accumulators in TMEM: G in columns 0..127, C S_hi in 128..191, C S_lo in 192..255, M X in 256..319 and
-// the state increment in 320..383; the increment is issued as soon as v o X is built and runs while the
-// threads build M.  A dedicated warp issues the copies and the products; the
-// element-wise work is split over the compute warpgroups (each warp reads the TMEM lanes of its quarter
-// of the rows).  The increment completes on a barrier of its own, so that the state update runs while
-// M X is still on the tensor cores.  A chunk's C is fetched as soon as the previous chunk's first product is done, its B and
-// X (and dt) as soon as the previous M X and increment are; y leaves through a TMA store of the tile staged
-// in M's place.
+// the state increment in 320..383.  A dedicated warp issues the copies and the products; four compute
+// warpgroups split the element-wise work (each warp reads the TMEM lanes of its quarter of the rows).
+// Overlaps within a chunk: the increment is issued as soon as v o X is built and runs while the threads
+// build M; it completes on a barrier of its own, so that the state update runs while M X is still on the
+// tensor cores.  Across chunks: the next chunk's C is fetched as soon as this chunk's first product is
+// done, its B, X and dt as soon as M X and the increment are; y leaves through a TMA store of the tile
+// staged in M's place.
 #include <cstdint>
 
 #include "bulk_copy.cuh"
