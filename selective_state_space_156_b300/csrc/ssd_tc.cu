@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sm + kOffX + 8192, &map_x, cc * kQ + 64, static_cast<int>(row0), bar_bx);
     };
 
+    bool c_pend_init = true;
     if (issuer) {
         *abort_flag = 0;
         mbar_init(bar_c, 1);
@@ -195,7 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&map_b);
         tma_prefetch_map(&map_x);
         tma_prefetch_map(&map_y);
-        issue_c(0);
+        if (a.withhold)
+            c_pend_init = false;   // test only: chunk 0's C is never copied, so every wait for it runs out
+        else
+            issue_c(0);
         issue_bx(0);
     }
     if (warp == 0) {
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
     // the issuer's view of its asynchronous work: issued and not yet seen complete by its own wait, with
     // the parity of the phase that completes it (a chunk's copies: the chunk's; products: their order)
-    bool c_pend = true, bx_pend = true, mma_pend = false, inc_pend = false;
+    bool c_pend = c_pend_init, bx_pend = true, mma_pend = false, inc_pend = false;
     unsigned c_par = 0, bx_par = 0, mma_par = 0, inc_par = 0;
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
@@ -516,7 +520,9 @@ cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     cudaError_t e = set_dynamic_smem_once(ssd_chunk_kernel, kSmemBytes);
     if (e != cudaSuccess) return e;
-    ssd_chunk_kernel<<<a.Bsz * a.H, kThreads, kSmemBytes, stream>>>(a, mc, mb, mx, my);
+    SsdArgs args = a;
+    args.withhold = withhold_first_copy() ? 1 : 0;
+    ssd_chunk_kernel<<<a.Bsz * a.H, kThreads, kSmemBytes, stream>>>(args, mc, mb, mx, my);
     return cudaGetLastError();
 }
 

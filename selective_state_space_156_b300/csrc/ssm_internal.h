@@ -148,9 +148,16 @@ struct SsdArgs {
     float* h_out;              // (B, H, 64, N) or NULL
     void* y;                   // (B, H*64, L) bf16
     int softplus, zoh;
+    int withhold;              // test only: chunk 0's C is never copied (every wait for it runs out)
 };
 
 bool ssd_tc_supported(int N, int P);
+
+// Test hook for the bounded waits, read on every launch: with SSM_TEST_WITHHOLD_FIRST_COPY=1 in the
+// environment, the streamed decode kernel (block 0) and the SSD kernel (every block) leave out their
+// first copy, so that waits for it run out after about a second and the kernel reports it through
+// ssm_device_error.  Nothing faults or hangs; the outputs of the affected tiles are left unwritten.
+bool withhold_first_copy();
 cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream);
 // The SSD kernel's flag for a copy or MMA it stopped waiting for.
 cudaError_t take_ssd_wait_error(unsigned* flags);

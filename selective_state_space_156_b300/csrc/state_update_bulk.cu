@@ -83,6 +83,7 @@ struct DecodeArgs {
     int W;
     const int* state_indices;  // (B) slot of each batch row in state / conv_state, or NULL (slot = b)
     int Bsz, D, softplus;
+    int withhold;              // test only: block 0 never copies its first tile (its waits run out)
 };
 
 template <typename T>
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                     atomicOr(&g_bulk_wait_error, 1u);
                     break;
                 }
+                if (a.withhold && blockIdx.x == 0 && j == 0) continue;   // no copy, no arrival: a wait runs out
                 const int t = (int)blockIdx.x + j * G;
                 const int b = t / tiles_per_b;
                 const int d0 = (t - b * tiles_per_b) * kTileRows;
@@ -363,7 +365,8 @@ bool state_update_bulk_eligible(const DecodeStep& s) {
 cudaError_t launch_state_update_bulk(const DecodeStep& s, cudaStream_t stream) {
     const DecodeArgs a{s.state, s.x, s.delta, s.A, s.Bm, s.Cm, s.Dskip, s.delta_bias, s.z, s.y,
                        s.conv_w, s.conv_w ? s.conv_b : nullptr, s.conv_w ? s.conv_state : nullptr,
-                       s.conv_w ? s.conv_width : 1, s.state_indices, s.Bsz, s.D, s.softplus};
+                       s.conv_w ? s.conv_width : 1, s.state_indices, s.Bsz, s.D, s.softplus,
+                       withhold_first_copy() ? 1 : 0};
     if (s.dtype == 1) return launch_bulk_t<BF16>(a, s.N, s.zoh, stream);
     return launch_bulk_t<F32>(a, s.N, s.zoh, stream);
 }

@@ -65,6 +65,11 @@ bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool withhold_first_copy() {
+    const char* v = std::getenv("SSM_TEST_WITHHOLD_FIRST_COPY");
+    return v != nullptr && v[0] == '1';
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* v = std::getenv("SSM_PDL");
