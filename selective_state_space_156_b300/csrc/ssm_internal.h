@@ -40,6 +40,7 @@ struct ScanKernelArgs {
     float* ws_h0;    // (B*D, N) copy of h0 taken before any block may write h_out (h0 may alias h_out)
     int kind;        // kScanSeq, kScanP16 or kScanG4
     int lpc;         // kScanP16: lanes per channel (1, 2 or 4)
+    int withhold;    // test only: block (0, 0) of the packed kernel's final pass never copies its first chunk
 };
 
 constexpr int kScanSeq = 0;  // one (b, d) row per thread, all states in registers (any dtype, any alignment)
@@ -154,8 +155,8 @@ struct SsdArgs {
 bool ssd_tc_supported(int N, int P);
 
 // Test hook for the bounded waits, read on every launch: with SSM_TEST_WITHHOLD_FIRST_COPY=1 in the
-// environment, the streamed decode kernel (block 0) and the SSD kernel (every block) leave out their
-// first copy, so that waits for it run out after about a second and the kernel reports it through
+// environment, the streamed decode kernel (block 0), the packed scan's TMA-staged final pass without an
+// L split (block (0, 0)) and the SSD kernel (every block) leave out their first copy, so that waits for it run out after about a second and the kernel reports it through
 // ssm_device_error.  Nothing faults or hangs; the outputs of the affected tiles are left unwritten.
 bool withhold_first_copy();
 cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream);

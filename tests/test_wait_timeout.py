@@ -1,6 +1,6 @@
 """The bounded waits, made to run out on a GPU: with SSM_TEST_WITHHOLD_FIRST_COPY=1 in the environment the
-streamed decode kernel and the SSD kernel leave out their first copy, so that the waits for it give up
-after about a second.  Nothing faults or hangs: the kernel records the failure, lets its other copies and
+packed scan (its TMA-staged pass), the streamed decode kernel and the SSD kernel leave out their first copy,
+so that the waits for it give up after about a second.  Nothing faults or hangs: the kernel records the failure, lets its other copies and
 products end, frees its tensor memory and returns; ssm_device_error reports the bit and clears it, and
 the same call without the switch is then correct, so the context stayed usable."""
 import os
@@ -29,6 +29,28 @@ def _withheld(call):
     finally:
         del os.environ[SWITCH]
     return flags
+
+
+def test_scan_wait_runs_out_and_is_reported():
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba1.4b_conv"], batch=2, dim=256, seqlen=304,
+                                   with_h0=True)
+    g = to_dev(d)
+
+    def run():
+        return ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], Dskip=g["Dskip"],
+                                delta_bias=g["delta_bias"], z=g["z"], conv_w=g["conv_w"], conv_b=g["conv_b"],
+                                h0=g["h0"], return_state=True, workspace=None)
+
+    flags = _withheld(run)
+    assert flags & 2, f"scan timeout not reported (flags {flags})"
+    y, h = run()
+    torch.cuda.synchronize()
+    assert ssm.ssm_device_error() == 0
+    ref_y, ref_h, _ = oracle.scan(d)
+    ref_y = ref_y.reshape(y.shape)
+    assert_close(y, ref_y, y_tolerance(ref_y, torch.bfloat16), "scan y after the timeout")
+    assert_close(h, ref_h.reshape(h.shape), h_tolerance(ref_h.reshape(h.shape), torch.bfloat16),
+                 "scan state after the timeout")
 
 
 def test_decode_wait_runs_out_and_is_reported():
@@ -69,6 +91,7 @@ def test_ssd_wait_runs_out_and_is_reported():
     torch.cuda.synchronize()
     assert ssm.ssm_device_error() == 0
     ref_y, ref_h, _ = ssd_scan(d)
-    assert_close(y, ref_y.reshape(y.shape), y_tolerance(ref_y, torch.bfloat16), "SSD y after the timeout")
+    ref_y = ref_y.reshape(y.shape)
+    assert_close(y, ref_y, y_tolerance(ref_y, torch.bfloat16), "SSD y after the timeout")
     assert_close(h, ref_h.reshape(h.shape), h_tolerance(ref_h.reshape(h.shape), torch.bfloat16),
                  "SSD state after the timeout")
