@@ -9,6 +9,8 @@
 //              dv += g E B;  dB += dBbar E;  dE = dBbar B;
 //              d(dt) += dAbar Abar a + dE dE/d(dt);  da += dAbar Abar dt + dE dE/da;  g <- Abar g
 //   with dE/d(dt) = Abar, dE/da = (dt Abar - E) / a (dt^2 / 2 at a = 0) for ZOH; 1 and 0 simplified.
+//   E and dE/da come from zoh_factor / zoh_factor_da: Taylor series where |x| < 2^-4, so that neither
+//   cancels as x -> 0.
 //
 // The states h_t come from the forward call's h_all (the state after every step, (B, L, D, N)): thread
 // (b, d) reads 64 contiguous bytes per step, consecutive threads consecutive rows.  Everything else (conv
@@ -59,7 +61,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
 
     // per-channel constants, as packed pairs of states (n, n + 1)
     f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2];
-    bool zero_a = false;
 #pragma unroll
     for (int p = 0; p < NS / 2; ++p) {
         float av[2], iv[2];
@@ -68,15 +69,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
             const int n = 2 * p + q;
             av[q] = (active && n < N) ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
             iv[q] = av[q] != 0.0f ? 1.0f / av[q] : 0.0f;
-            zero_a |= active && n < N && av[q] == 0.0f;
         }
         a2[p] = pack2(av[0], av[1]);
         al2[p] = pack2(av[0] * kLog2e, av[1] * kLog2e);
         inva2[p] = pack2(iv[0], iv[1]);
     }
-    // a block with some A == 0 takes the element-wise form of the zero-order-hold factor (its a -> 0
-    // limit) in every step; the others the packed form
-    const bool safe = kZOH && __syncthreads_or(zero_a);
     float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
     if (kConv && active) {
         const int W = a.conv_width;
@@ -264,27 +261,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 for (int p = 0; p < NS / 2; ++p) {
                     g2[p] = fma2(Ct[p], dyss2, g2[p]);
                     red2[8 + p] = mul2(dyss2, hcur[p]);                 // dC contribution
-                    const f32x2 Ab = ex2x2(mul2(dt2, al2[p]));
+                    const f32x2 y2 = mul2(dt2, al2[p]);
+                    const f32x2 Ab = ex2x2(y2);
                     f32x2 E, dEdt, dEda;
                     if (!kZOH) {
                         E = dt2;
                         dEdt = one2;
                         dEda = pack2(0.0f, 0.0f);
-                    } else if (!safe) {
-                        E = mul2(sub2(Ab, one2), inva2[p]);
-                        dEdt = Ab;
-                        dEda = mul2(sub2(mul2(dt2, Ab), E), inva2[p]);
-                    } else {  // some A == 0 in the block: the a -> 0 limits E = dt, dE/da = dt^2 / 2
-                        float ab0, ab1, av0, av1, iv0, iv1;
+                    } else {
+                        // exact forms (zoh_factor, zoh_factor_da): Taylor series where |dt a| < 2^-4, where
+                        // (Abar - 1) / a and (dt Abar - E) / a would cancel; the limits dt and dt^2 / 2 at a = 0
+                        float ab0, ab1, av0, av1, iv0, iv1, y0, y1;
                         unpack2(Ab, ab0, ab1);
                         unpack2(a2[p], av0, av1);
                         unpack2(inva2[p], iv0, iv1);
-                        const float E0 = av0 != 0.0f ? (ab0 - 1.0f) * iv0 : dt;
-                        const float E1 = av1 != 0.0f ? (ab1 - 1.0f) * iv1 : dt;
+                        unpack2(y2, y0, y1);
+                        const float E0 = zoh_factor(dt, y0, ab0, iv0);
+                        const float E1 = zoh_factor(dt, y1, ab1, iv1);
                         E = pack2(E0, E1);
                         dEdt = Ab;
-                        dEda = pack2(av0 != 0.0f ? (dt * ab0 - E0) * iv0 : 0.5f * dt * dt,
-                                     av1 != 0.0f ? (dt * ab1 - E1) * iv1 : 0.5f * dt * dt);
+                        dEda = pack2(zoh_factor_da(dt, dt * av0, ab0, E0, iv0), zoh_factor_da(dt, dt * av1, ab1, E1, iv1));
                     }
                     const f32x2 dAb = mul2(g2[p], hprev[p]);
                     const f32x2 dBb = mul2(g2[p], v2);

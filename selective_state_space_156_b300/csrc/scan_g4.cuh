@@ -157,16 +157,13 @@ __device__ __forceinline__ void g4_group(const ScanKernelArgs& a, G4Smem<NSL>& s
                 const f32x2 ng = mul2(mul2(v2, cc.ninva[p]), Bp[p]);
                 hp[p] = fma2(ab, sub2(hp[p], ng), ng);
             }
-        } else {  // Bbar = ((Abar - 1) / a + [a == 0] dt) B = ([a == 0] dt - (Abar - 1) ninva) B
+        } else {  // exact: h' = Abar h + E v B (E from the series where |dt a| < 2^-4; dt at a = 0)
 #pragma unroll
             for (int p = 0; p < NSL / 2; ++p) {
-                const f32x2 ab = ex2x2(mul2(dt2, cc.al2[p]));
-                float n0, n1, d0_, d1_;
-                unpack2(cc.ninva[p], n0, n1);
-                unpack2(dt2, d0_, d1_);
-                const f32x2 zdt = pack2(n0 == 0.0f ? d0_ : 0.0f, n1 == 0.0f ? d1_ : 0.0f);
-                const f32x2 phi = sub2(zdt, mul2(sub2(ab, pack2(1.0f, 1.0f)), cc.ninva[p]));
-                hp[p] = fma2(ab, hp[p], mul2(mul2(phi, Bp[p]), v2));
+                const f32x2 y2 = mul2(dt2, cc.al2[p]);
+                const f32x2 ab = ex2x2(y2);
+                const f32x2 E = zoh_factor2(dt2, y2, ab, cc.ninva[p]);
+                hp[p] = fma2(ab, hp[p], mul2(E, mul2(v2, Bp[p])));
             }
         }
         if (kFinal) {
@@ -261,7 +258,7 @@ __global__ void __launch_bounds__(kG4Threads, 7) scan_g4_kernel(const ScanKernel
     g4_issue_chunk<NSL>(a, sm, 0, b, ch0, t_begin, has_z);
 
     G4Consts<NSL> cc;
-    bool has_zero = false;
+    bool small_a = false;  // some state with |A| < kZohFastMinA (0 included): the exact form
 #pragma unroll
     for (int p = 0; p < NSL / 2; ++p) {
         float al[2], ni[2];
@@ -272,7 +269,7 @@ __global__ void __launch_bounds__(kG4Threads, 7) scan_g4_kernel(const ScanKernel
             const float av = real ? __ldg(a.A + (size_t)d * a.N + n) : 0.0f;
             al[e] = av * kLog2e;
             ni[e] = av != 0.0f ? -1.0f / av : 0.0f;
-            has_zero |= real && av == 0.0f;
+            small_a |= real && !(fabsf(av) >= kZohFastMinA);
         }
         cc.al2[p] = pack2(al[0], al[1]);
         cc.ninva[p] = pack2(ni[0], ni[1]);
@@ -325,7 +322,7 @@ __global__ void __launch_bounds__(kG4Threads, 7) scan_g4_kernel(const ScanKernel
     f32x2 hp[NSL / 2];
 #pragma unroll
     for (int p = 0; p < NSL / 2; ++p) hp[p] = pack2(h[2 * p], h[2 * p + 1]);
-    const bool safe = kZOH && __any_sync(0xffffffffu, has_zero);
+    const bool exact = kZOH && __any_sync(0xffffffffu, small_a);  // warp-uniform choice of loop body
 
     int buf = 0;
     for (int c0 = t_begin; c0 < t_end; c0 += kG4Chunk, buf ^= 1) {
@@ -374,8 +371,8 @@ __global__ void __launch_bounds__(kG4Threads, 7) scan_g4_kernel(const ScanKernel
         __syncthreads();
         const int clen = min(kG4Chunk, t_end - c0);
         for (int j0 = 0; j0 < clen; j0 += 8) {
-            if (safe)
-                g4_group<NSL, Disc::kZOHSafe, kFinal, kConv>(a, sm, buf, warp, g, q, cl, j0, cc, hp, dsum, has_z);
+            if (exact)
+                g4_group<NSL, Disc::kZOHExact, kFinal, kConv>(a, sm, buf, warp, g, q, cl, j0, cc, hp, dsum, has_z);
             else
                 g4_group<NSL, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv>(a, sm, buf, warp, g, q, cl, j0, cc, hp,
                                                                               dsum, has_z);

@@ -14,9 +14,8 @@
 // which is the segment state passing of pwwt.cn/news/5168881 section 3.1 done in parallel.
 //
 // Zero-order hold, per state n with a = A[d, n], x = dt a, Abar = 2^(x log2 e):
-//   Bbar v = (Abar - 1) / a * B v.  Writing g = (v / a) B gives h' = Abar (h + g) - g, whose fixed
-//   point for a constant input is exactly -g = -B v / a, whatever the rounding of Abar.
-// A warp in which some a == 0 takes a second loop body that uses the a -> 0 limit dt * B instead.
+//   h' = Abar h + E B v,  E = (exp(x) - 1) / a  (zoh_factor: the Taylor series of expm1(x) / x below
+//   |x| = 2^-4, where (Abar - 1) / a would cancel, and the quotient above; dt at a = 0).
 #pragma once
 
 #include "ssm_device.cuh"
@@ -34,7 +33,6 @@ template <int NS>
 struct ChannelConsts {
     float al2[NS];   // A[d, n] * log2(e); 0 for padded n >= N
     float inva[NS];  // 1 / A[d, n]; 0 for padded n and for A == 0
-    float zmask[NS]; // 1 where A[d, n] == 0 (n < N), else 0
     float w[4];      // conv taps aligned so w[3] multiplies x_t
     float cb, dskip, bias;
 };
@@ -104,24 +102,13 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
                     else y0 = fmaf(Ct[n], h[n], y0);
                 }
             }
-        } else if (kDisc == Disc::kZOH) {
+        } else {  // zero-order hold, exact form: Bbar = E B with E from zoh_factor (any a, a = 0 included)
 #pragma unroll
             for (int n = 0; n < NS; ++n) {
-                float ab = ex2(dtj * cc.al2[n]);
-                float gq = (vj * cc.inva[n]) * Bt[n];
-                float s = h[n] + gq;
-                h[n] = fmaf(ab, s, -gq);
-                if (kFinal) {
-                    if (n & 1) y1 = fmaf(Ct[n], h[n], y1);
-                    else y0 = fmaf(Ct[n], h[n], y0);
-                }
-            }
-        } else {  // kZOHSafe: Bbar = ((Abar - 1) / a + [a == 0] dt) B
-#pragma unroll
-            for (int n = 0; n < NS; ++n) {
-                float ab = ex2(dtj * cc.al2[n]);
-                float phi = fmaf(ab - 1.0f, cc.inva[n], cc.zmask[n] * dtj);
-                h[n] = fmaf(ab, h[n], phi * Bt[n] * vj);
+                const float y = dtj * cc.al2[n];
+                const float ab = ex2(y);
+                const float E = zoh_factor(dtj, y, ab, cc.inva[n]);
+                h[n] = fmaf(ab, h[n], E * (Bt[n] * vj));
                 if (kFinal) {
                     if (n & 1) y1 = fmaf(Ct[n], h[n], y1);
                     else y0 = fmaf(Ct[n], h[n], y0);
@@ -208,15 +195,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
                                                                   : nullptr;
 
     ChannelConsts<NS> cc;
-    bool has_zero = false;
 #pragma unroll
     for (int n = 0; n < NS; ++n) {
         const float av = (active && n < a.N) ? __ldg(a.A + (size_t)d * a.N + n) : 0.0f;
-        const bool real = active && n < a.N;
         cc.al2[n] = av * kLog2e;
         cc.inva[n] = (av != 0.0f) ? 1.0f / av : 0.0f;
-        cc.zmask[n] = (real && av == 0.0f) ? 1.0f : 0.0f;
-        has_zero |= real && av == 0.0f;
     }
     cc.w[0] = cc.w[1] = cc.w[2] = cc.w[3] = 0.0f;
     cc.cb = 0.0f;
@@ -273,12 +256,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
             if (n < a.N) a.ws_h0[row * a.N + n] = a.h0[row * a.N + n];
     }
 
-    constexpr Disc kMain = kZOH ? Disc::kZOH : Disc::kSimple;
+    // the fp32 path always takes the exact zero-order hold (its bound 1e-4 (1 + |y|) leaves no room for
+    // the fast form's error at small |A|)
+    constexpr Disc kMain = kZOH ? Disc::kZOHExact : Disc::kSimple;
     const bool run = active && !pad;
-    if (kZOH && __any_sync(0xffffffffu, has_zero))
-        scan_segment<Tin, Tout, NS, Disc::kZOHSafe, kFinal>(a, sh, run, b, row, t_begin, t_end, cc, h, xh, dsum, hall);
-    else
-        scan_segment<Tin, Tout, NS, kMain, kFinal>(a, sh, run, b, row, t_begin, t_end, cc, h, xh, dsum, hall);
+    scan_segment<Tin, Tout, NS, kMain, kFinal>(a, sh, run, b, row, t_begin, t_end, cc, h, xh, dsum, hall);
 
     if (!active) return;
     if (pad) {  // a padding row: y is zero, no slot is touched

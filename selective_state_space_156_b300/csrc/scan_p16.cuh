@@ -15,8 +15,10 @@
 //
 // Zero-order hold per state pair, with ninv = -1/a and ng = (v ninv) B = -(v/a) B:
 //   h' = Abar (h - ng) + ng  ==  Abar h + (Abar - 1)(v/a) B,
-// whose fixed point for a constant input is -ng exactly, whatever the rounding of Abar.  A block in
-// which some a == 0 runs a second loop body that uses the a -> 0 limit dt B (lshu.cn/news/79586 2.2).
+// whose fixed point for a constant input is -ng exactly, whatever the rounding of Abar.  Its error per
+// step grows as |v B / a|, so a block in which some state has |a| < kZohFastMinA (a == 0 included) runs
+// a second loop body, h' = Abar h + E v B with E = (exp(dt a) - 1) / a from zoh_factor2 (a Taylor series
+// where |dt a| is small, the limit dt at a = 0; lshu.cn/news/79586 2.2).
 //
 // Staging.  Per 48-step chunk, five tiled bulk tensor copies (TMA, issued by one thread, completing on
 // an mbarrier) bring the block's u/x rows (with an 8-step halo for the conv front end of
@@ -229,18 +231,16 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int p = p4 + q;
-                const f32x2 ab = ex2x2(mul2(dt2, cc.al2[p]));
+                const f32x2 y2 = mul2(dt2, cc.al2[p]);
+                const f32x2 ab = ex2x2(y2);
                 if (kDisc == Disc::kSimple) {
                     hp[p] = fma2(ab, hp[p], mul2(mul2(dt2, v2), Bp[q]));
                 } else if (kDisc == Disc::kZOH) {
                     const f32x2 ng = mul2(mul2(v2, cc.ninv[p]), Bp[q]);
                     hp[p] = fma2(ab, sub2(hp[p], ng), ng);
-                } else {  // Bbar = ([a == 0] dt - (Abar - 1) ninv) B
-                    float n0, n1;
-                    unpack2(cc.ninv[p], n0, n1);
-                    const f32x2 zdt = pack2(n0 == 0.0f ? dtj : 0.0f, n1 == 0.0f ? dtj : 0.0f);
-                    const f32x2 phi = sub2(zdt, mul2(sub2(ab, pack2(1.0f, 1.0f)), cc.ninv[p]));
-                    hp[p] = fma2(ab, hp[p], mul2(mul2(phi, Bp[q]), v2));
+                } else {  // exact: h' = Abar h + E v B (E from the series where |dt a| < 2^-4; dt at a = 0)
+                    const f32x2 E = zoh_factor2(dt2, y2, ab, cc.ninv[p]);
+                    hp[p] = fma2(ab, hp[p], mul2(E, mul2(v2, Bp[q])));
                 }
             }
             if (kFinal) {
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
     }
 
     P16Consts<NSL> cc;
-    bool has_zero = false;
+    bool small_a = false;  // some state with |A| < kZohFastMinA (0 included): the exact form
 #pragma unroll
     for (int p = 0; p < NSL / 2; ++p) {
         float al[2], ni[2];
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
             const float av = real ? __ldg(a.A + (size_t)d * a.N + n) : 0.0f;
             al[q] = av * kLog2e;
             ni[q] = av != 0.0f ? -1.0f / av : 0.0f;
-            has_zero |= real && av == 0.0f;
+            small_a |= real && !(fabsf(av) >= kZohFastMinA);
         }
         cc.al2[p] = pack2(al[0], al[1]);
         cc.ninv[p] = pack2(ni[0], ni[1]);
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
 #pragma unroll
     for (int p = 0; p < NSL / 2; ++p) hp[p] = pack2(h[2 * p], h[2 * p + 1]);
 
-    const bool safe = kZOH && __syncthreads_or(has_zero);  // block-uniform choice of loop body
+    const bool exact = kZOH && __syncthreads_or(small_a);  // block-uniform choice of loop body
     const size_t yoff = row * (size_t)a.L;
 
     int buf = 0, k = 0;
@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
             float* hall = kHall ? a.h_all + ((size_t)b * a.L * a.D + (active ? d : 0)) * a.N + e * NSL +
                                           (size_t)c0 * a.D * a.N
                                 : nullptr;
-            if (safe)
-                p16_group<NS, LPC, Disc::kZOHSafe, kFinal, kConv, kHall>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum,
+            if (exact)
+                p16_group<NS, LPC, Disc::kZOHExact, kFinal, kConv, kHall>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum,
                                                                           has_z, active, yoff + c0, hall);
             else
                 p16_group<NS, LPC, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv, kHall>(

@@ -10,9 +10,63 @@ namespace ssm {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Discretisation of the input term: zero-order hold, zero-order hold with A == 0 entries present in
-// the warp (uses the dt * B limit there), or the simplified dt * B.
-enum class Disc { kZOH, kZOHSafe, kSimple };
+// Discretisation of the input term: zero-order hold in the fast form (for blocks whose every state
+// has |A| >= kZohFastMinA), zero-order hold in the exact form (any A, including 0), or the
+// simplified dt * B.
+enum class Disc { kZOH, kZOHExact, kSimple };
+
+// ---------------------------------------------------------------------------------------------
+// Zero-order hold input factor E = (exp(x) - 1) / a, x = dt a (dpshk.com/news/3333417 section 2.2,
+// lshu.cn/news/79586 section 2.2, diagonal A), so that Bbar = E B.
+//
+// Formed as (Abar - 1) / a, E loses log2(1/|x|) bits to cancellation: Abar carries an absolute
+// error of about 2^-23 near 1, so E's relative error is about 1.2e-7 / |x|.  Below |x| = 2^-4 the
+// exact form is used instead: E = dt phi(x), phi(x) = expm1(x) / x = sum_k x^k / (k+1)!, summed
+// by Horner to the x^3 term (truncation x^4 / 120 < 1.3e-7 relative at |x| = 2^-4).  Above the
+// threshold (Abar - 1) / a is within about 4e-6 relative.  At a = 0 the series gives the limit dt.
+// The series and the threshold are written from the Taylor expansion of exp, not from any library.
+// ---------------------------------------------------------------------------------------------
+constexpr float kZohSeriesX = 0.0625f;              // |x| below which E comes from the series
+constexpr float kZohSeriesY = 0.0625f * kLog2e;     // the same threshold for y = x log2(e)
+// phi(x) = 1 + x/2 + x^2/6 + x^3/24 written in y = x log2 e: coefficients (ln 2)^k / (k+1)!
+constexpr float kPhiY1 = 0.34657359027997264f;      // ln2 / 2
+constexpr float kPhiY2 = 0.08007550231970023f;      // ln2^2 / 6
+constexpr float kPhiY3 = 0.013876027166205394f;     // ln2^3 / 24
+// Blocks (warps) in which every state has |A| at least this may use the fast form
+// h' = Abar (h - ng) + ng, ng = -(v / a) B: its absolute error per step is about 2^-22 |v B / a|, so
+// over the at most 64 k steps that a state remembers it stays near 2.5e-4 |v B| for |A| >= 1/4, within
+// the bf16-path state bound 1e-3 (1 + |h|).  The fp32 path always takes the exact form.
+constexpr float kZohFastMinA = 0.25f;
+
+// phi(x) in terms of y = x log2 e (|y| < kZohSeriesY).
+__device__ __forceinline__ float zoh_phi_y(float y) {
+    float p = fmaf(y, kPhiY3, kPhiY2);
+    p = fmaf(p, y, kPhiY1);
+    return fmaf(p, y, 1.0f);
+}
+
+// E for one state: y = dt a log2 e, ab = 2^y, inva = 1 / a (0 where a == 0).
+__device__ __forceinline__ float zoh_factor(float dt, float y, float ab, float inva) {
+    const float big = (ab - 1.0f) * inva;
+    const float small = dt * zoh_phi_y(y);
+    return fabsf(y) < kZohSeriesY ? small : big;
+}
+
+// dE/da for the backward pass: (dt Abar - E) / a, which cancels twice as x -> 0 (dt Abar - E is about
+// dt x / 2), so below |x| = 1/4 it is dt^2 phi'(x), phi'(x) = sum_k k x^(k-1) / (k+1)!
+// = 1/2 + x/3 + x^2/8 + x^3/30 + x^4/144 + x^5/840 (truncation x^6 / 5760 < 1e-7 relative at |x| = 1/4);
+// above, the quotient is within about 1e-5 relative.
+constexpr float kZohDaSeriesX = 0.25f;
+__device__ __forceinline__ float zoh_factor_da(float dt, float x, float ab, float E, float inva) {
+    const float big = fmaf(dt, ab, -E) * inva;
+    float p = fmaf(x, 1.0f / 840.0f, 1.0f / 144.0f);
+    p = fmaf(p, x, 1.0f / 30.0f);
+    p = fmaf(p, x, 0.125f);
+    p = fmaf(p, x, 1.0f / 3.0f);
+    p = fmaf(p, x, 0.5f);
+    const float small = dt * dt * p;
+    return fabsf(x) < kZohDaSeriesX ? small : big;
+}
 
 // 2^x on the MUFU unit (ex2.approx.ftz: about 2 ulp, 32 results per clock per SM on B300).
 __device__ __forceinline__ float ex2(float x) {
@@ -118,6 +172,21 @@ __device__ __forceinline__ f32x2 ex2x2(f32x2 x) {
     float a, b;
     unpack2(x, a, b);
     return pack2(ex2(a), ex2(b));
+}
+
+// zoh_factor on a pair of states, given ninv2 = -1/a (0 where a == 0): series and quotient both on
+// packed pairs, the choice per state.
+__device__ __forceinline__ f32x2 zoh_factor2(f32x2 dt2, f32x2 y2, f32x2 ab2, f32x2 ninv2) {
+    f32x2 p = fma2(y2, pack2(kPhiY3, kPhiY3), pack2(kPhiY2, kPhiY2));
+    p = fma2(p, y2, pack2(kPhiY1, kPhiY1));
+    p = fma2(p, y2, pack2(1.0f, 1.0f));
+    const f32x2 small = mul2(p, dt2);
+    const f32x2 big = mul2(sub2(pack2(1.0f, 1.0f), ab2), ninv2);
+    float y0, y1, s0, s1, b0, b1;
+    unpack2(y2, y0, y1);
+    unpack2(small, s0, s1);
+    unpack2(big, b0, b1);
+    return pack2(fabsf(y0) < kZohSeriesY ? s0 : b0, fabsf(y1) < kZohSeriesY ? s1 : b1);
 }
 
 // ---------------------------------------------------------------------------------------------

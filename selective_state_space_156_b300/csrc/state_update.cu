@@ -45,8 +45,8 @@ __device__ __forceinline__ void load4<BF16>(const void* base, size_t i, bool vec
 // two halves of a sector), and every lane keeps 32 bytes of the HBM stream in flight.  A, B and C of
 // those states come in with 16-byte (A) and 8-byte (bf16 B, C) loads.  The per-row scalars (dt, v)
 // are computed by both lanes; the readout is summed over the two lanes with one shuffle and lane 0
-// applies the D skip and the gate.  Zero-order hold as in the scan: h' = Abar (h - ng) + ng with
-// ng = -(v / a) B, exact at the fixed point; a == 0 uses the limit dt B.
+// applies the D skip and the gate.  Zero-order hold in the exact form h' = Abar h + E v B, with
+// E = (exp(dt a) - 1) / a from zoh_factor (a Taylor series where |dt a| is small, dt at a = 0).
 template <typename T, int NSL, bool kZOH, bool kConv>
 __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeStep s, int vec) {
     float* __restrict__ state = s.state;
@@ -138,14 +138,11 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
 #pragma unroll
     for (int i = 0; i < NSL; ++i) {
         const float a = av[i];
-        const float ab = ex2(dt * (a * kLog2e));
-        if (kZOH) {
-            if (a != 0.0f) {
-                const float ng = (uv * -rcp(a)) * Bt[i];
-                h[i] = fmaf(ab, h[i] - ng, ng);
-            } else {
-                h[i] = fmaf(dt * uv, Bt[i], h[i]);  // the a -> 0 limit: Abar = 1, Bbar = dt B
-            }
+        const float y = dt * (a * kLog2e);
+        const float ab = ex2(y);
+        if (kZOH) {  // exact form: E from the series where |dt a| < 2^-4, dt at a = 0
+            const float E = zoh_factor(dt, y, ab, a != 0.0f ? rcp(a) : 0.0f);
+            h[i] = fmaf(ab, h[i], E * (uv * Bt[i]));
         } else {
             h[i] = fmaf(ab, h[i], (dt * uv) * Bt[i]);
         }

@@ -243,6 +243,12 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                     h[4 * c] = hv.x; h[4 * c + 1] = hv.y; h[4 * c + 2] = hv.z; h[4 * c + 3] = hv.w;
                     A4[4 * c] = av.x; A4[4 * c + 1] = av.y; A4[4 * c + 2] = av.z; A4[4 * c + 3] = av.w;
                 }
+                // bf16 I/O: warps whose states all have |A| >= kZohFastMinA take the fast zero-order-hold
+                // form (its error is far inside the bf16 bound there); fp32 I/O always the exact form
+                bool small_a = false;
+#pragma unroll
+                for (int i = 0; i < SL; ++i) small_a |= !(fabsf(A4[i]) >= kZohFastMinA);
+                const bool exact = T::kBytes != 2 || __any_sync(0xffffffffu, small_a);
                 float uv = smem_scalar<T>(st + L::kOffU, r);
                 if constexpr (kConv) {
                     // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}); x before t is the row's conv state
@@ -280,13 +286,16 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
                 float yp = 0.0f;
 #pragma unroll
                 for (int i = 0; i < SL; ++i) {
-                    const float ab = ex2(dt * (A4[i] * kLog2e));
-                    if (kZOH) {
-                        // branch-free: the a -> 0 limit (Abar = 1, Bbar = dt B) is selected, not branched to
-                        const bool nz = A4[i] != 0.0f;
-                        const float ng = nz ? (uv * -rcp(A4[i])) * Bv[i] : 0.0f;
-                        const float hz = fmaf(ab, h[i] - ng, ng);
-                        h[i] = nz ? hz : fmaf(dtu, Bv[i], h[i]);
+                    const float y = dt * (A4[i] * kLog2e);
+                    const float ab = ex2(y);
+                    if (kZOH && exact) {
+                        // exact form, branch-free: E from the series where |dt a| < 2^-4 (dt at a = 0)
+                        const float E = zoh_factor(dt, y, ab, A4[i] != 0.0f ? rcp(A4[i]) : 0.0f);
+                        h[i] = fmaf(ab, h[i], E * (uv * Bv[i]));
+                    } else if (kZOH) {
+                        // fast form h' = Abar (h - ng) + ng, ng = -(v / a) B (every |a| >= 1/4 in the warp)
+                        const float ng = (uv * -rcp(A4[i])) * Bv[i];
+                        h[i] = fmaf(ab, h[i] - ng, ng);
                     } else {
                         h[i] = fmaf(ab, h[i], dtu * Bv[i]);
                     }
