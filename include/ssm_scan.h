@@ -156,7 +156,9 @@ SSM_API ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream);
  * caller still provides every input and output.
  *   - The buffer lives in each device's memory from the first use until the process exits.
  *   - The first call on a device looks up the buffer's device address (once per device, with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The address is looked up
+ *     again when the device's current context is no longer the one it was taken in (for example after
+ *     cudaDeviceReset); such a call, too, should come before any stream capture.
  *   - Every call shares the one buffer per device: calls whose kernels may overlap on the GPU
  *     (different streams, or several host threads) race on it and must be serialised by the caller.
  *   - A problem whose split needs more than 4 MiB of scratch is rejected with SSM_ERR_UNSUPPORTED
@@ -271,6 +273,17 @@ SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
  * Errors: SSM_ERR_INVALID_ARG (flags NULL), SSM_ERR_CUDA (the synchronisation or the read failed).
  */
 SSM_API ssm_status ssm_device_error(unsigned *flags);
+
+/*
+ * Test hook, not for production use.  (No counterpart on the pages.)  With on != 0, later calls of the
+ * packed scan's single-pass launch (block (0, 0)), the streamed decode kernel (block 0) and the SSD
+ * kernel (every block) leave out their first staged copy, so that their bounded waits for it run out
+ * after about a second and ssm_device_error reports bits 1, 0 and 2; the outputs of those blocks are
+ * then not written.  on == 0 (the state at load) restores normal operation.  A process-wide flag read at
+ * each launch; setting it while another thread launches is allowed (the launch sees the old or the new
+ * value).  No errors.
+ */
+SSM_API void ssm_test_withhold_first_copy(int on);
 
 /*
  * Single-token decode step with the conv front end fused: the decode cache holds a conv state and

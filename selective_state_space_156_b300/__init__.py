@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), vp]
         L.ssm_device_error.restype = st
         L.ssm_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.ssm_test_withhold_first_copy.restype = None
+        L.ssm_test_withhold_first_copy.argtypes = [i]
         L.ssm_last_error.restype = ctypes.c_char_p
         L.ssm_last_error.argtypes = []
         L.ssm_version.restype = ctypes.c_char_p
@@ -361,6 +363,12 @@ def ssm_device_error() -> int:
     flags = ctypes.c_uint(0)
     _check(lib().ssm_device_error(ctypes.byref(flags)))
     return int(flags.value)
+
+
+def ssm_test_withhold_first_copy(on: bool) -> None:
+    """Test hook: while on, the packed scan, streamed decode and SSD kernels leave out their first staged
+    copy so that their bounded waits run out (see ssm_device_error).  Never for production use."""
+    lib().ssm_test_withhold_first_copy(1 if on else 0)
 
 
 def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,

@@ -80,13 +80,19 @@ KindGeom kind_geom(int kind, int lpc) {
 }
 
 // Lanes per channel of the packed kernel.  More lanes per channel give more warps (better latency
-// hiding) at a higher per-step cost; SSM_SCAN_LANES_PER_CHANNEL (1, 2 or 4) overrides the choice.
+// hiding) at a higher per-step cost.  SSM_SCAN_LANES_PER_CHANNEL (1, 2 or 4), read once per process,
+// overrides the choice (for comparisons).
+int lpc_override() {
+    static const int v = [] {
+        const char* env = getenv("SSM_SCAN_LANES_PER_CHANNEL");
+        const int x = env != nullptr ? atoi(env) : 0;
+        return (x == 1 || x == 2 || x == 4) ? x : 0;
+    }();
+    return v;
+}
+
 int choose_lpc(const ssm_scan_params* p) {
-    if (const char* env = getenv("SSM_SCAN_LANES_PER_CHANNEL")) {
-        const int v = atoi(env);
-        if (v == 1 || v == 2 || v == 4) return p->dstate <= 4 ? 1 : (p->dstate <= 8 && v > 2 ? 2 : v);
-    }
-    (void)p;
+    if (const int v = lpc_override()) return p->dstate <= 4 ? 1 : (p->dstate <= 8 && v > 2 ? 2 : v);
     return 1;  // measured fastest on the 8 x 4096 x 16 x 2048 and 1 x 5120 x 16 x 65536 workloads
 }
 
@@ -239,6 +245,24 @@ constexpr int kStaticScratchMaxDevices = 64;
 
 std::mutex g_static_scratch_mu;
 void* g_static_scratch_addr[kStaticScratchMaxDevices] = {};
+void* g_static_scratch_ctx[kStaticScratchMaxDevices] = {};  // the context the address was taken in
+
+// The calling thread's current driver context (cuCtxGetCurrent, looked up through the runtime so that
+// the library does not link against libcuda), or nullptr when it cannot be had.
+void* current_context() {
+    using Fn = int (*)(void**);
+    static Fn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<Fn>(p);
+        return static_cast<Fn>(nullptr);
+    }();
+    void* ctx = nullptr;
+    if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
 
 }  // namespace
 
@@ -257,12 +281,16 @@ ssm_status static_scratch_address(void** out) {
         return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd_static: device %d is beyond the %d devices it tracks", dev,
                     kStaticScratchMaxDevices);
     std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-    if (g_static_scratch_addr[dev] == nullptr) {
+    // asked again when the device's context is not the one the address was taken in (after a
+    // cudaDeviceReset the module is loaded anew and the old address is stale)
+    void* ctx = current_context();
+    if (g_static_scratch_addr[dev] == nullptr || ctx == nullptr || ctx != g_static_scratch_ctx[dev]) {
         void* addr = nullptr;
         e = cudaGetSymbolAddress(&addr, ssm_static_scratch);
         if (e != cudaSuccess) return cuda_status(e, "ssm_scan_fwd_static: cudaGetSymbolAddress");
         if (addr == nullptr) return fail(SSM_ERR_CUDA, "ssm_scan_fwd_static: no device address for the scratch buffer");
         g_static_scratch_addr[dev] = addr;
+        g_static_scratch_ctx[dev] = current_context();
     }
     *out = g_static_scratch_addr[dev];
     return SSM_OK;

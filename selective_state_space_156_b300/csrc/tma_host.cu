@@ -1,6 +1,7 @@
 // Host side of the tiled bulk-tensor copies: the driver's tensor-map encoder, looked up once through the
 // runtime so that the library does not link against libcuda; and the once-per-kernel shared-memory
 // attribute of the kernels that use more than 48 KB.
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -65,10 +66,18 @@ bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool withhold_first_copy() {
-    const char* v = std::getenv("SSM_TEST_WITHHOLD_FIRST_COPY");
-    return v != nullptr && v[0] == '1';
+// Test hook (ssm_test_withhold_first_copy): set only by the bounded-wait tests, off otherwise.
+static std::atomic<int> g_withhold_first_copy{0};
+
+bool withhold_first_copy() { return g_withhold_first_copy.load(std::memory_order_relaxed) != 0; }
+
+}  // namespace ssm
+
+extern "C" SSM_API void ssm_test_withhold_first_copy(int on) {
+    ssm::g_withhold_first_copy.store(on ? 1 : 0, std::memory_order_relaxed);
 }
+
+namespace ssm {
 
 bool pdl_enabled() {
     static const bool on = [] {

@@ -1,10 +1,8 @@
-"""The bounded waits, made to run out on a GPU: with SSM_TEST_WITHHOLD_FIRST_COPY=1 in the environment the
+"""The bounded waits, made to run out on a GPU: with the library's test hook ssm_test_withhold_first_copy on, the
 packed scan (its TMA-staged pass), the streamed decode kernel and the SSD kernel leave out their first copy,
 so that the waits for it give up after about a second.  Nothing faults or hangs: the kernel records the failure, lets its other copies and
 products end, frees its tensor memory and returns; ssm_device_error reports the bit and clears it, and
 the same call without the switch is then correct, so the context stayed usable."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -17,17 +15,14 @@ from oracle.ssd import ssd_scan
 
 pytestmark = pytest.mark.gpu
 
-SWITCH = "SSM_TEST_WITHHOLD_FIRST_COPY"
-
-
 def _withheld(call):
     assert ssm.ssm_device_error() == 0
-    os.environ[SWITCH] = "1"
+    ssm.ssm_test_withhold_first_copy(True)
     try:
         call()
         flags = ssm.ssm_device_error()   # synchronises the device
     finally:
-        del os.environ[SWITCH]
+        ssm.ssm_test_withhold_first_copy(False)
     return flags
 
 

@@ -3,14 +3,15 @@ that plans every buffer at start-up, code in a stream callback, latency-critical
 allocation may synchronise the device).  It takes the scratch of the L split from a fixed 4 MiB buffer
 inside the library instead of a caller workspace.
 
-Checked through the C ABI against ssm_scan_fwd with a workspace, on two calls in a row (the buffer keeps
-the previous call's contents), on two problems of different shapes, and for the rejection of a problem
-whose split needs more than the buffer.  Collected last so that a run stopping at its first failure has
+Checked through the C ABI against ssm_scan_fwd with a workspace and against the fp64 oracle element by
+element, on two calls in a row (the buffer keeps the previous call's contents), on two problems of
+different shapes, and for the rejection of a problem whose split needs more than the buffer.  Collected last so that a run stopping at its first failure has
 run every other test first; it also passes on its own in a fresh process."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import selective_state_space_156_b300 as ssm
 import workloads
 from gpu_helpers import assert_close, h_tolerance, to_dev, y_tolerance
@@ -43,6 +44,9 @@ def test_static_scratch_matches_workspace_entry_point_twice(case):
     torch.cuda.synchronize()
     yr = y_ref.double().cpu().numpy()
     hr = h_ref.double().cpu().numpy()
+    yo, ho, _ = oracle.scan(d)
+    yo = yo.reshape(yr.shape)
+    ho = ho.reshape(hr.shape)
     y = torch.empty_like(y_ref)
     h = torch.empty_like(h_ref)
     for call in range(2):
@@ -52,6 +56,8 @@ def test_static_scratch_matches_workspace_entry_point_twice(case):
         torch.cuda.synchronize()
         assert_close(y, yr, y_tolerance(yr, y.dtype), f"y, call {call}")
         assert_close(h, hr, h_tolerance(hr, g["u"].dtype), f"h_out, call {call}")
+        assert_close(y, yo, y_tolerance(yo, y.dtype), f"y against the oracle, call {call}")
+        assert_close(h, ho, h_tolerance(ho, g["u"].dtype), f"h_out against the oracle, call {call}")
 
 
 def test_static_scratch_rejects_a_split_beyond_the_buffer():
