@@ -595,12 +595,16 @@ def run_other_configs(ssm, dev, skip: str, hbm_peak: float, fp32_peak: float, mu
             pieces = [{k: g[k][..., a:a + cfg.chunk].contiguous() for k in ("u", "delta", "z", "Bm", "Cm")}
                       for a in range(0, cfg.seqlen, cfg.chunk)]
             yp = torch.empty_like(pieces[0]["u"])
+            p0 = pieces[0]
+            wsc = ssm.ssm_scan_workspace_size(p0["u"], p0["delta"], g["A"], p0["Bm"], p0["Cm"], h0=h, h_out=h, y=yp,
+                                              **dict(kw, z=p0["z"]))
+            wsc = torch.empty(max(wsc, 1), dtype=torch.uint8, device=dev)
 
             def chained():
                 h.zero_()
                 for pc in pieces:
                     ssm.ssm_scan_fwd(pc["u"], pc["delta"], g["A"], pc["Bm"], pc["Cm"], h0=h, h_out=h, y=yp,
-                                     **dict(kw, z=pc["z"]))
+                                     workspace=wsc, **dict(kw, z=pc["z"]))
             variants[f"{cfg.seqlen // cfg.chunk} chained calls"] = chained
         res = {}
         for vname, fn in variants.items():

@@ -230,7 +230,7 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
                  conv_b: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
                  h_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
                  delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
-                 workspace: Optional[torch.Tensor] = None, return_state: bool = False, stream=None,
+                 workspace="auto", return_state: bool = False, stream=None,
                  conv_init: Optional[torch.Tensor] = None, conv_final: Optional[torch.Tensor] = None,
                  state_indices: Optional[torch.Tensor] = None, h_all: Optional[torch.Tensor] = None):
     """Selective scan forward on the GPU.  Layouts as in include/ssm_scan.h: u/delta/z/y (B, D, L),
@@ -238,9 +238,10 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
     h0/h_out (B, D, N) fp32, conv_init/conv_final (B, D, W-1) of u's dtype (the conv history before
     and after this call; conv_final may be conv_init).  ``state_indices`` (B,) int32 makes h0, h_out,
     conv_init and conv_final slot caches indexed per batch row (negative: padding row, y = 0);
-    ``h_all`` (B, L, D, N) fp32 receives the state after every step.  ``workspace`` (uint8 CUDA tensor,
-    optional) enables the L split; pass ``workspace="auto"`` to allocate it here.  Returns y, or
-    (y, h_out) with return_state."""
+    ``h_all`` (B, L, D, N) fp32 receives the state after every step.  ``workspace``: "auto" (default)
+    allocates, through torch's allocator, the scratch that lets the library split L when the (b, d) rows
+    alone would leave the GPU idle; a uint8 CUDA tensor of at least ssm_scan_workspace_size bytes; or
+    None (no split).  Returns y, or (y, h_out) with return_state."""
     if y is None:
         y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
     if return_state and h_out is None:

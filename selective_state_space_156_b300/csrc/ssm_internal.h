@@ -154,10 +154,11 @@ struct SsdArgs {
 
 bool ssd_tc_supported(int N, int P);
 
-// Test hook for the bounded waits, read on every launch: with SSM_TEST_WITHHOLD_FIRST_COPY=1 in the
-// environment, the streamed decode kernel (block 0), the packed scan's TMA-staged final pass without an
-// L split (block (0, 0)) and the SSD kernel (every block) leave out their first copy, so that waits for it run out after about a second and the kernel reports it through
-// ssm_device_error.  Nothing faults or hangs; the outputs of the affected tiles are left unwritten.
+// Test hook for the bounded waits (ssm_test_withhold_first_copy, a process-wide flag read at each launch):
+// while set, the streamed decode kernel (block 0), the packed scan's TMA-staged final pass without an L
+// split (block (0, 0)) and the SSD kernel (every block) leave out their first copy, so that waits for it
+// run out after about a second and the kernel reports it through ssm_device_error.  Nothing faults or
+// hangs; the outputs of the affected tiles are left unwritten.
 bool withhold_first_copy();
 cudaError_t launch_ssd_chunked(const SsdArgs& a, cudaStream_t stream);
 // The SSD kernel's flag for a copy or MMA it stopped waiting for.
