@@ -112,6 +112,13 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  *                   state at the accepted length (pwwt.cn/news/5168881 section 3.4: speculative
  *                   decoding).  Takes the element-wise kernel (dstate <= 16); must not overlap any
  *                   other tensor; padding rows leave theirs untouched.
+ *   h_ckpt      (B, ceil(L / SSM_CKPT_STEPS), D, N) float32, or NULL: receives one state every
+ *                   SSM_CKPT_STEPS steps, entry c being the state after step min(8c + 7, L - 1): the
+ *                   checkpoints from which ssm_scan_bwd recomputes the states it needs, instead of
+ *                   keeping every state (the states saved for the backward pass of
+ *                   dpshk.com/news/3333417 section 5.3, with the gradient checkpointing of
+ *                   pwwt.cn/news/5168881 section 3.2).  Not together with h_all or state_indices;
+ *                   dstate <= 16; must not overlap any other tensor.
  */
 typedef struct ssm_scan_params {
     int batch, dim, dstate, seqlen;
@@ -138,7 +145,11 @@ typedef struct ssm_scan_params {
     void *conv_final;
     const int *state_indices;
     float *h_all;
+    float *h_ckpt;
 } ssm_scan_params;
+
+/* Steps between the forward's state checkpoints (h_ckpt) that the backward pass recomputes from. */
+#define SSM_CKPT_STEPS 8
 
 /* Selective scan forward (with the optional fused conv front end, D skip and gate).
    Errors: SSM_ERR_INVALID_ARG (null p, null required pointer, size <= 0, bad dtype/flag value,
@@ -202,7 +213,10 @@ SSM_API ssm_status ssm_state_update(float *state, const void *u, const void *del
  * Forward inputs (batch, dim, dstate, seqlen, in_dtype, u, delta, A, Bm, Cm, Dskip, delta_bias, z,
  * conv_w, conv_b, conv_width, conv_init, h0, delta_softplus, zoh) are exactly those of the forward
  * call, and
- *   h_all    (B, L, D, N) float32  the forward's state after every step (ssm_scan_fwd with h_all)  required
+ *   h_ckpt   (B, ceil(L/8), D, N) float32  the forward's state checkpoints (ssm_scan_fwd with h_ckpt)  required;
+ *            the pass reloads the checkpoint before each group of 8 steps and recomputes the group's
+ *            states from it (with the inputs, dt, Abar and the zero-order-hold factor), so the forward
+ *            never stores every state
  *   dy       (B, D, L) in_dtype    gradient of y                                                  required
  *   dh_out   (B, D, N) float32     gradient of the final state, or NULL for zero
  * Outputs (element-wise ones in in_dtype, the rest float32; each may be NULL only where its input was):
@@ -236,7 +250,7 @@ typedef struct ssm_scan_bwd_params {
     const float *h0;
     int delta_softplus;
     int zoh;
-    const float *h_all;
+    const float *h_ckpt;
     const void *dy;
     const float *dh_out;
     void *du;

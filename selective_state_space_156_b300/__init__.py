@@ -10,7 +10,7 @@ Entry points (same names as the C ABI):
   causal_conv1d_fwd(x, w, b=None, silu=True)  -> y
   ssm_state_update(state, u, delta, A, Bm, Cm, ...)  -> y  (state updated in place)
   ssm_scan_workspace_size(...)                -> bytes of optional scratch for the L split
-  ssm_scan_bwd(u, delta, A, Bm, Cm, dy, h_all, ...) -> gradients of every input
+  ssm_scan_bwd(u, delta, A, Bm, Cm, dy, h_ckpt, ...) -> gradients of every input
   ssd_scan_fwd(x, dt, A, Bm, Cm, nheads=..., ngroups=...) -> y (Mamba-2 / SSD layer, tensor cores)
 """
 from __future__ import annotations
@@ -48,7 +48,7 @@ class ScanParams(ctypes.Structure):
         ("h_out", ctypes.c_void_p), ("y", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
         ("zoh", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("conv_init", ctypes.c_void_p), ("conv_final", ctypes.c_void_p),
-        ("state_indices", ctypes.c_void_p), ("h_all", ctypes.c_void_p),
+        ("state_indices", ctypes.c_void_p), ("h_all", ctypes.c_void_p), ("h_ckpt", ctypes.c_void_p),
     ]
 
 
@@ -61,7 +61,7 @@ class ScanBwdParams(ctypes.Structure):
         ("Cm", ctypes.c_void_p), ("Dskip", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p), ("z", ctypes.c_void_p),
         ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("conv_width", ctypes.c_int),
         ("conv_init", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
-        ("zoh", ctypes.c_int), ("h_all", ctypes.c_void_p), ("dy", ctypes.c_void_p), ("dh_out", ctypes.c_void_p),
+        ("zoh", ctypes.c_int), ("h_ckpt", ctypes.c_void_p), ("dy", ctypes.c_void_p), ("dh_out", ctypes.c_void_p),
         ("du", ctypes.c_void_p), ("ddelta", ctypes.c_void_p), ("dz", ctypes.c_void_p), ("dA", ctypes.c_void_p),
         ("dB", ctypes.c_void_p), ("dC", ctypes.c_void_p), ("dDskip", ctypes.c_void_p),
         ("ddelta_bias", ctypes.c_void_p), ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p),
@@ -166,8 +166,17 @@ def _slots_shape(t, name, Bsz, tail, state_indices):
     return tuple(t.shape)
 
 
+CKPT_STEPS = 8  # SSM_CKPT_STEPS: steps between the forward's state checkpoints
+
+
+def ckpt_count(seqlen: int) -> int:
+    """Entries of the checkpoint tensor h_ckpt for a sequence of seqlen steps: ceil(seqlen / 8)."""
+    return (seqlen + CKPT_STEPS - 1) // CKPT_STEPS
+
+
 def _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
-                 workspace, conv_init=None, conv_final=None, state_indices=None, h_all=None) -> ScanParams:
+                 workspace, conv_init=None, conv_final=None, state_indices=None, h_all=None,
+                 h_ckpt=None) -> ScanParams:
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
     Bsz, D, L = u.shape
@@ -203,6 +212,7 @@ def _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, 
     p.h_out = _ptr(h_out, "h_out", torch.float32, _slots_shape(h_out, "h_out", Bsz, (D, N), state_indices))
     p.state_indices = _ptr(state_indices, "state_indices", torch.int32, (Bsz,))
     p.h_all = _ptr(h_all, "h_all", torch.float32, (Bsz, L, D, N))
+    p.h_ckpt = _ptr(h_ckpt, "h_ckpt", torch.float32, (Bsz, ckpt_count(L), D, N))
     p.y = _ptr(y, "y", None, (Bsz, D, L)) if y is not None else None
     p.delta_softplus = int(bool(delta_softplus))
     p.zoh = int(bool(zoh))
@@ -220,7 +230,7 @@ def ssm_scan_workspace_size(u, delta, A, Bm, Cm, **kw) -> int:
     p = _scan_params(u, delta, A, Bm, Cm, kw.get("Dskip"), kw.get("delta_bias"), kw.get("z"), kw.get("conv_w"),
                      kw.get("conv_b"), kw.get("h0"), kw.get("h_out"), y, kw.get("delta_softplus", True),
                      kw.get("zoh", True), None, kw.get("conv_init"), kw.get("conv_final"), kw.get("state_indices"),
-                     kw.get("h_all"))
+                     kw.get("h_all"), kw.get("h_ckpt"))
     return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
 
 
@@ -232,13 +242,16 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
                  delta_softplus: bool = True, zoh: bool = True, out_dtype: Optional[torch.dtype] = None,
                  workspace="auto", return_state: bool = False, stream=None,
                  conv_init: Optional[torch.Tensor] = None, conv_final: Optional[torch.Tensor] = None,
-                 state_indices: Optional[torch.Tensor] = None, h_all: Optional[torch.Tensor] = None):
+                 state_indices: Optional[torch.Tensor] = None, h_all: Optional[torch.Tensor] = None,
+                 h_ckpt: Optional[torch.Tensor] = None):
     """Selective scan forward on the GPU.  Layouts as in include/ssm_scan.h: u/delta/z/y (B, D, L),
     Bm/Cm (B, N, L), A (D, N) fp32, Dskip/delta_bias/conv_b (D,) fp32, conv_w (D, W) fp32,
     h0/h_out (B, D, N) fp32, conv_init/conv_final (B, D, W-1) of u's dtype (the conv history before
     and after this call; conv_final may be conv_init).  ``state_indices`` (B,) int32 makes h0, h_out,
     conv_init and conv_final slot caches indexed per batch row (negative: padding row, y = 0);
-    ``h_all`` (B, L, D, N) fp32 receives the state after every step.  ``workspace``: "auto" (default)
+    ``h_all`` (B, L, D, N) fp32 receives the state after every step; ``h_ckpt`` (B, ckpt_count(L), D, N) fp32
+    the state after every 8th step (and after the last), the checkpoints ssm_scan_bwd recomputes from.
+    ``workspace``: "auto" (default)
     allocates, through torch's allocator, the scratch that lets the library split L when the (b, d) rows
     alone would leave the GPU idle; a uint8 CUDA tensor of at least ssm_scan_workspace_size bytes; or
     None (no split).  Returns y, or (y, h_out) with return_state."""
@@ -252,10 +265,10 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
         n = ssm_scan_workspace_size(u, delta, A, Bm, Cm, Dskip=Dskip, delta_bias=delta_bias, z=z, conv_w=conv_w,
                                     conv_b=conv_b, h0=h0, h_out=h_out, y=y, delta_softplus=delta_softplus, zoh=zoh,
                                     conv_init=conv_init, conv_final=conv_final, state_indices=state_indices,
-                                    h_all=h_all)
+                                    h_all=h_all, h_ckpt=h_ckpt)
         workspace = torch.empty(n, dtype=torch.uint8, device=u.device) if n > 0 else None
     p = _scan_params(u, delta, A, Bm, Cm, Dskip, delta_bias, z, conv_w, conv_b, h0, h_out, y, delta_softplus, zoh,
-                     workspace, conv_init, conv_final, state_indices, h_all)
+                     workspace, conv_init, conv_final, state_indices, h_all, h_ckpt)
     _check(lib().ssm_scan_fwd(ctypes.byref(p), _stream(stream)))
     return (y, h_out) if return_state else y
 
@@ -373,15 +386,16 @@ def ssm_test_withhold_first_copy(on: bool) -> None:
 
 
 def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
-                 dy: torch.Tensor, h_all: torch.Tensor, Dskip: Optional[torch.Tensor] = None,
+                 dy: torch.Tensor, h_ckpt: torch.Tensor, Dskip: Optional[torch.Tensor] = None,
                  delta_bias: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
                  conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
                  conv_init: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
                  dh_out: Optional[torch.Tensor] = None, delta_softplus: bool = True, zoh: bool = True,
                  stream=None, workspace="auto") -> dict:
     """Backward pass of ssm_scan_fwd: gradients of sum(y * dy) + sum(h_L * dh_out) for every input, keyed
-    like the inputs (``u`` is the gradient of x with a conv; ``h0`` that of the initial state).  ``h_all``
-    (B, L, D, N) fp32 is the forward call's state after every step (ssm_scan_fwd with h_all=...).
+    like the inputs (``u`` is the gradient of x with a conv; ``h0`` that of the initial state).  ``h_ckpt``
+    (B, ckpt_count(L), D, N) fp32 holds the forward call's state checkpoints (ssm_scan_fwd with h_ckpt=...);
+    the pass recomputes the other states from them.
     ``workspace``: "auto" (allocated here when the L split pays), None (no split) or a uint8 tensor."""
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
@@ -425,7 +439,7 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, Bm: torc
     p.h0 = _ptr(h0, "h0", torch.float32, (Bsz, D, N))
     p.delta_softplus = int(bool(delta_softplus))
     p.zoh = int(bool(zoh))
-    p.h_all = _ptr(h_all, "h_all", torch.float32, (Bsz, L, D, N))
+    p.h_ckpt = _ptr(h_ckpt, "h_ckpt", torch.float32, (Bsz, ckpt_count(L), D, N))
     p.dy = _ptr(dy, "dy", idt, (Bsz, D, L))
     p.dh_out = _ptr(dh_out, "dh_out", torch.float32, (Bsz, D, N))
     p.du, p.ddelta, p.dz = _ptr(g["u"], "du"), _ptr(g["delta"], "ddelta"), _ptr(g["z"], "dz")

@@ -59,9 +59,10 @@ int scan_kind(const ssm_scan_params* p) {
     // state slots are implemented by the element-wise kernel; the per-step state output by it and by the
     // packed kernel (16-byte-aligned h_all)
     if (p->state_indices != nullptr) return ssm::kScanSeq;
+    const float* hs = p->h_all != nullptr ? p->h_all : p->h_ckpt;  // the state output (every step or every 8th)
     if (p->in_dtype == SSM_BF16 && p->out_dtype == SSM_BF16 && aligned_rows(p)) {
-        if (p->dstate <= 16 && (p->h_all == nullptr || aligned16(p->h_all))) return ssm::kScanP16;
-        if (p->dstate <= 64 && p->h_all == nullptr) return ssm::kScanG4;
+        if (p->dstate <= 16 && (hs == nullptr || aligned16(hs))) return ssm::kScanP16;
+        if (p->dstate <= 64 && hs == nullptr) return ssm::kScanG4;
     }
     return ssm::kScanSeq;
 }
@@ -158,10 +159,14 @@ ssm_status validate_scan(const ssm_scan_params* p) {
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: delta_softplus and zoh must be 0 or 1");
     if (p->conv_w != nullptr && (p->conv_width < 1 || p->conv_width > 4))
         return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: conv_width %d outside 1..4", p->conv_width);
+    if (p->h_all != nullptr && p->h_ckpt != nullptr)
+        return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_all and h_ckpt are alternatives (give one)");
+    if (p->h_ckpt != nullptr && p->state_indices != nullptr)
+        return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: h_ckpt is not offered with state_indices");
     if (!dstate_supported(p))
         return fail(SSM_ERR_UNSUPPORTED,
                     "ssm_scan_fwd: dstate %d not supported (1..16; 32 and 64 need bf16 in/out, 16-byte-aligned "
-                    "rows, seqlen %% 8 == 0 and neither state_indices nor h_all)", p->dstate);
+                    "rows, seqlen %% 8 == 0 and none of state_indices, h_all, h_ckpt)", p->dstate);
     const size_t rows = (size_t)p->batch * p->dim;
     if (rows * (size_t)p->seqlen >= ((size_t)1 << 40))
         return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: batch*dim*seqlen too large");
@@ -183,6 +188,16 @@ ssm_status validate_scan(const ssm_scan_params* p) {
             (p->h_out && !p->state_indices && overlaps(p->h_all, hb, p->h_out, rows * p->dstate * 4)) ||
             (p->h0 && !p->state_indices && overlaps(p->h_all, hb, p->h0, rows * p->dstate * 4)))
             return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_all overlaps another tensor");
+    }
+    if (p->h_ckpt != nullptr) {
+        const size_t ck = (size_t)(p->seqlen + SSM_CKPT_STEPS - 1) / SSM_CKPT_STEPS;
+        const size_t hb = rows * ck * (size_t)p->dstate * 4;
+        if (overlaps(p->h_ckpt, hb, p->u, nbdl * ib) || overlaps(p->h_ckpt, hb, p->delta, nbdl * ib) ||
+            overlaps(p->h_ckpt, hb, p->z, nbdl * ib) || overlaps(p->h_ckpt, hb, p->Bm, nbnl * ib) ||
+            overlaps(p->h_ckpt, hb, p->Cm, nbnl * ib) || overlaps(p->h_ckpt, hb, p->y, ybytes) ||
+            (p->h_out && overlaps(p->h_ckpt, hb, p->h_out, rows * p->dstate * 4)) ||
+            (p->h0 && overlaps(p->h_ckpt, hb, p->h0, rows * p->dstate * 4)))
+            return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: h_ckpt overlaps another tensor");
     }
     if (p->conv_w != nullptr && p->conv_width > 1 && p->state_indices == nullptr) {
         const size_t cbytes = rows * (size_t)(p->conv_width - 1) * ib;
@@ -213,7 +228,8 @@ ssm::ScanKernelArgs scan_args(const ssm_scan_params* p) {
     a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr; a.conv_width = p->conv_w ? p->conv_width : 0;
     a.conv_init = (p->conv_w && p->conv_width > 1) ? p->conv_init : nullptr;
     a.state_indices = p->state_indices;
-    a.h_all = p->h_all;
+    a.h_all = p->h_all != nullptr ? p->h_all : p->h_ckpt;
+    a.hall_every = p->h_ckpt != nullptr ? SSM_CKPT_STEPS : 1;
     a.h0 = p->h0; a.h_out = p->h_out; a.y = p->y;
     a.softplus = p->delta_softplus;
     a.vec = aligned_rows(p);
@@ -349,9 +365,9 @@ ssm_status validate_bwd(const ssm_scan_bwd_params* p) {
     if (p->in_dtype != SSM_F32 && p->in_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "%s: bad dtype", who);
     if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->zoh != 0 && p->zoh != 1))
         return fail(SSM_ERR_INVALID_ARG, "%s: delta_softplus and zoh must be 0 or 1", who);
-    if (!p->u || !p->delta || !p->A || !p->Bm || !p->Cm || !p->h_all || !p->dy || !p->du || !p->ddelta || !p->dA ||
+    if (!p->u || !p->delta || !p->A || !p->Bm || !p->Cm || !p->h_ckpt || !p->dy || !p->du || !p->ddelta || !p->dA ||
         !p->dB || !p->dC)
-        return fail(SSM_ERR_INVALID_ARG, "%s: u, delta, A, Bm, Cm, h_all, dy, du, ddelta, dA, dB and dC are required",
+        return fail(SSM_ERR_INVALID_ARG, "%s: u, delta, A, Bm, Cm, h_ckpt, dy, du, ddelta, dA, dB and dC are required",
                     who);
     if (p->z && !p->dz) return fail(SSM_ERR_INVALID_ARG, "%s: dz is required with z", who);
     if (p->conv_w && (p->conv_width < 1 || p->conv_width > 4))
@@ -361,7 +377,8 @@ ssm_status validate_bwd(const ssm_scan_bwd_params* p) {
     const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
     struct Range { const void* p; size_t n; };
     const Range ins[] = {{p->u, nbdl * eb}, {p->delta, nbdl * eb}, {p->z, nbdl * eb}, {p->Bm, nbnl * eb},
-                         {p->Cm, nbnl * eb}, {p->dy, nbdl * eb}, {p->h_all, nbdl * p->dstate * 4},
+                         {p->Cm, nbnl * eb}, {p->dy, nbdl * eb},
+                         {p->h_ckpt, rows * (size_t)((p->seqlen + SSM_CKPT_STEPS - 1) / SSM_CKPT_STEPS) * p->dstate * 4},
                          {p->A, (size_t)p->dim * p->dstate * 4}, {p->h0, rows * p->dstate * 4}};
     const Range outs[] = {{p->du, nbdl * eb}, {p->ddelta, nbdl * eb}, {p->dz, nbdl * eb},
                           {p->dA, (size_t)p->dim * p->dstate * 4}, {p->dB, nbnl * 4}, {p->dC, nbnl * 4},
@@ -402,7 +419,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
     a.delta_bias = p->delta_bias; a.z = p->z; a.conv_w = p->conv_w; a.conv_b = p->conv_w ? p->conv_b : nullptr;
     a.conv_width = p->conv_w ? p->conv_width : 0;
     a.conv_init = (p->conv_w && p->conv_width > 1) ? p->conv_init : nullptr;
-    a.h0 = p->h0; a.h_all = p->h_all; a.dy = p->dy; a.dh_out = p->dh_out;
+    a.h0 = p->h0; a.h_ckpt = p->h_ckpt; a.dy = p->dy; a.dh_out = p->dh_out;
     a.du = p->du; a.ddelta = p->ddelta; a.dz = p->z ? p->dz : nullptr; a.dA = p->dA; a.dB = p->dB; a.dC = p->dC;
     a.dDskip = p->Dskip ? p->dDskip : nullptr; a.ddelta_bias = p->delta_bias ? p->ddelta_bias : nullptr;
     a.dconv_w = p->conv_w ? p->dconv_w : nullptr; a.dconv_b = (p->conv_w && p->conv_b) ? p->dconv_b : nullptr;

@@ -9,12 +9,15 @@
 //              dv += g E B;  dB += dBbar E;  dE = dBbar B;
 //              d(dt) += dAbar Abar a + dE dE/d(dt);  da += dAbar Abar dt + dE dE/da;  g <- Abar g
 //   with dE/d(dt) = Abar, dE/da = (dt Abar - E) / a (dt^2 / 2 at a = 0) for ZOH; 1 and 0 simplified.
-//   E and dE/da come from zoh_factor / zoh_factor_da: Taylor series where |x| < 2^-4, so that neither
-//   cancels as x -> 0.
+//   E and dE/da come from zoh_factor2 / zoh_factor_da2 (packed pairs): Taylor series where |x| is small,
+//   so that neither cancels as x -> 0.
 //
-// The states h_t come from the forward call's h_all (the state after every step, (B, L, D, N)): thread
-// (b, d) reads 64 contiguous bytes per step, consecutive threads consecutive rows.  Everything else (conv
-// front end, dt, Abar, E) is recomputed from the inputs.  dB and dC are sums over the channels of a batch
+// The states h_t are recomputed from the forward call's checkpoints (h_ckpt: the state after every 8th
+// step, (B, ceil(L/8), D, N); the gradient checkpointing of pwwt.cn/news/5168881 section 3.2 in place of
+// keeping every state): before each group of 8 steps, thread (b, d) reloads the checkpoint that precedes
+// it (64 contiguous bytes) and runs the group's recurrence forward again, keeping the 8 states in shared
+// memory, then walks them in reverse.  Everything else (conv front end, dt, Abar, E) is recomputed from
+// the inputs.  dB and dC are sums over the channels of a batch
 // row: per step each warp transposes its lanes' contributions through shared memory and sums them, and
 // after a group of 8 steps the block adds its four warp sums to global memory with one atomic per (b, n,
 // t).  Per-channel parameter gradients (dA, D skip, dt bias, conv taps and bias) accumulate over time in
@@ -29,6 +32,12 @@ namespace {
 constexpr int kBwdThreads = 128;
 constexpr int kBwdChunk = 64;   // steps of B / C staged per chunk
 constexpr int kBwdGroup = 8;    // steps per group (vector loads / stores, one reduction flush)
+constexpr int kCkpt = SSM_CKPT_STEPS;  // steps per forward checkpoint: one group
+static_assert(kCkpt == kBwdGroup, "a group starts right after a checkpoint");
+
+// Dynamic shared memory of the backward kernel: the group's recomputed states.
+template <int NS>
+constexpr int bwd_state_smem() { return kBwdGroup * NS * kBwdThreads * (int)sizeof(float); }
 
 template <int NS>
 struct BwdShared {
@@ -60,7 +69,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     const int t1 = min(L, t0 + a.seg_len);
 
     // per-channel constants, as packed pairs of states (n, n + 1)
-    f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2];
+    f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2], ninv2[NS / 2];
 #pragma unroll
     for (int p = 0; p < NS / 2; ++p) {
         float av[2], iv[2];
@@ -73,6 +82,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
         a2[p] = pack2(av[0], av[1]);
         al2[p] = pack2(av[0] * kLog2e, av[1] * kLog2e);
         inva2[p] = pack2(iv[0], iv[1]);
+        ninv2[p] = pack2(-iv[0], -iv[1]);
     }
     float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
     if (kConv && active) {
@@ -111,51 +121,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     float dD = 0.0f, dbias = 0.0f, dw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dcb = 0.0f;
     float px[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // pending dx of x_t, x_{t-1}, x_{t-2}, x_{t-3}
 
-    // h_t of the step being processed; starts at h_{L-1}
-    const size_t hstride = (size_t)a.D * N;  // h_all: (B, L, D, N)
-    const float* hrow = a.h_all + ((size_t)b * L * a.D + dd) * N;
-    // states as packed pairs; whole 16-byte rows of h_all load as pairs directly
-    const bool hvec = (N == NS) && ((reinterpret_cast<uintptr_t>(a.h_all) & 15) == 0);
-    auto load_h = [&](int t, f32x2 (&hp)[NS / 2]) {
-        if (hvec && active) {
-            const ulonglong2* q = reinterpret_cast<const ulonglong2*>(hrow + (size_t)t * hstride);
-#pragma unroll
-            for (int k = 0; k < NS / 4; ++k) {
-                const ulonglong2 w2 = __ldcs(q + k);
-                hp[2 * k] = w2.x;
-                hp[2 * k + 1] = w2.y;
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < NS / 2; ++p) {
-                float hv[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    hv[q] = (active && 2 * p + q < N) ? hrow[(size_t)t * hstride + 2 * p + q] : 0.0f;
-                hp[p] = pack2(hv[0], hv[1]);
-            }
-        }
-    };
-    // h_{t}, the state of the step being processed, and a ring of the next two earlier states (h_{t-1},
-    // h_{t-2}) loaded ahead so that the load latency overlaps two steps of work; before t = 0 it is h0
-    auto fetch = [&](int t, f32x2 (&hp)[NS / 2]) {
-        if (t >= 0) {
-            load_h(t, hp);
-        } else {
-#pragma unroll
-            for (int p = 0; p < NS / 2; ++p) {
-                float hv[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    hv[q] = (t == -1 && a.h0 && active && 2 * p + q < N) ? a.h0[row * N + 2 * p + q] : 0.0f;
-                hp[p] = pack2(hv[0], hv[1]);
-            }
-        }
-    };
-    f32x2 hcur[NS / 2], ring0[NS / 2], ring1[NS / 2];
-    load_h(t1 - 1, hcur);
-    fetch(t1 - 2, ring0);
-    fetch(t1 - 3, ring1);
+    // The group's states h_tg .. h_tg+7, recomputed from the checkpoint before the group, live in
+    // dynamic shared memory as [step j][quad q][thread] float4s (conflict-free 16-byte accesses); the
+    // state before the group, h_{tg-1}, stays in registers.
+    extern __shared__ float4 bwd_hs[];
+    auto hs_at = [&](int j, int q) -> float4& { return bwd_hs[(j * (NS / 4) + q) * kBwdThreads + tid]; };
+    const int nck = (L + kCkpt - 1) / kCkpt;
+    const float* crow = a.h_ckpt + ((size_t)b * nck * a.D + dd) * N;  // entry c: the state after step 8c + 7
+    const size_t cstride = (size_t)a.D * N;
 
     const int last_chunk = t0 + ((t1 - 1 - t0) / kBwdChunk) * kBwdChunk;
     for (int c0 = last_chunk; c0 >= t0; c0 -= kBwdChunk) {
@@ -205,15 +178,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     else if (active && a.conv_init && t >= -W1) xh[k] = load1<Tin>(a.conv_init, row * W1 + W1 + t);
                 }
             }
-            float du_o[kBwdGroup], dd_o[kBwdGroup], dz_o[kBwdGroup];
+            // per-step scalars of the group: SSM input v (conv pre-activation c), step dt
+            float vv[kBwdGroup], cv[kBwdGroup], sv[kBwdGroup], dtv[kBwdGroup];
 #pragma unroll
-            for (int j = kBwdGroup - 1; j >= 0; --j) {
-                du_o[j] = dd_o[j] = dz_o[j] = 0.0f;
-                if (j >= nv) continue;  // uniform over the block: nv is
-                const int t = tg + j;
-                // recompute the step's scalars
-                float v, c = 0.0f, xm[4];
+            for (int j = 0; j < kBwdGroup; ++j) {
+                float c = 0.0f, v;
                 if (kConv) {
+                    float xm[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int m = j - 3 + k;  // x_{t-3+k}
@@ -227,16 +198,90 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 } else {
                     v = xv[j];
                 }
-                const float s = dv[j] + bias;
-                const float dt = a.softplus ? softplus(s) : s;
-                // h_{t-1} from the ring; the ring moves on and fetches h_{t-3}
-                f32x2 hprev[NS / 2];
+                cv[j] = c;
+                vv[j] = v;
+                sv[j] = dv[j] + bias;
+                dtv[j] = a.softplus ? softplus(sv[j]) : sv[j];
+            }
+            // the state before the group (the previous group's checkpoint, or h0), then the group's states
+            // recomputed forward from it with the forward pass's zero-order hold (exact form)
+            f32x2 hstart[NS / 2], hcur[NS / 2];
+            {
+                const float* src = tg > 0 ? crow + (size_t)(tg / kCkpt - 1) * cstride : a.h0 ? a.h0 + row * N : nullptr;
+                // src is NULL before t = 0 without h0: the state is zero, nothing is read
+                const bool vec4 = src != nullptr && (N == NS) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+                if (vec4 && active) {
+                    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(src);
 #pragma unroll
-                for (int p = 0; p < NS / 2; ++p) {
-                    hprev[p] = ring0[p];
-                    ring0[p] = ring1[p];
+                    for (int k = 0; k < NS / 4; ++k) {
+                        const ulonglong2 w2 = __ldcs(q + k);
+                        hstart[2 * k] = w2.x;
+                        hstart[2 * k + 1] = w2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        float hv[2];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) hv[q] = (src && active && 2 * p + q < N) ? src[2 * p + q] : 0.0f;
+                        hstart[p] = pack2(hv[0], hv[1]);
+                    }
                 }
-                if (t - 3 >= -1) fetch(t - 3, ring1);
+#pragma unroll
+                for (int p = 0; p < NS / 2; ++p) hcur[p] = hstart[p];
+#pragma unroll
+                for (int j = 0; j < kBwdGroup; ++j) {
+                    if (j >= nv) break;  // uniform over the block
+                    const f32x2* Bt = reinterpret_cast<const f32x2*>(sh.bc[0][tg + j - c0]);
+                    const f32x2 dt2 = pack2(dtv[j], dtv[j]), v2 = pack2(vv[j], vv[j]);
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        const f32x2 y2 = mul2(dt2, al2[p]);
+                        const f32x2 Ab = ex2x2(y2);
+                        f32x2 E = dt2;
+                        if (kZOH) E = zoh_factor2(dt2, y2, Ab, ninv2[p]);
+                        hcur[p] = fma2(Ab, hcur[p], mul2(E, mul2(v2, Bt[p])));
+                    }
+#pragma unroll
+                    for (int k = 0; k < NS / 4; ++k) {
+                        float h0_, h1_, h2_, h3_;
+                        unpack2(hcur[2 * k], h0_, h1_);
+                        unpack2(hcur[2 * k + 1], h2_, h3_);
+                        hs_at(j, k) = make_float4(h0_, h1_, h2_, h3_);
+                    }
+                }
+            }
+            float du_o[kBwdGroup], dd_o[kBwdGroup], dz_o[kBwdGroup];
+            // not unrolled: the step body is large (eight state pairs), and eight copies of it overflow the
+            // instruction cache (4.86 -> 4.48 ms on the 8 x 4096 x 16 x 2048 layer); the per-step arrays
+            // indexed by j live in local memory (L1)
+#pragma unroll 1
+            for (int j = kBwdGroup - 1; j >= 0; --j) {
+                du_o[j] = dd_o[j] = dz_o[j] = 0.0f;
+                if (j >= nv) continue;  // uniform over the block: nv is
+                const int t = tg + j;
+                const float v = vv[j], c = cv[j], s = sv[j], dt = dtv[j];
+                float xm[4];
+                if (kConv) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int m = j - 3 + k;  // x_{t-3+k}
+                        xm[k] = m >= 0 ? xv[m >= 0 ? m : 0] : xh[m + 3 >= 0 ? m + 3 : 0];
+                    }
+                }
+                // h_t (in hcur since the previous step, or from the forward recompute) and h_{t-1}
+                f32x2 hprev[NS / 2];
+                if (j > 0) {
+#pragma unroll
+                    for (int k = 0; k < NS / 4; ++k) {
+                        const float4 f = hs_at(j - 1, k);
+                        hprev[2 * k] = pack2(f.x, f.y);
+                        hprev[2 * k + 1] = pack2(f.z, f.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) hprev[p] = hstart[p];
+                }
                 const f32x2* Bt = reinterpret_cast<const f32x2*>(sh.bc[0][t - c0]);
                 const f32x2* Ct = reinterpret_cast<const f32x2*>(sh.bc[1][t - c0]);
                 f32x2 yacc = pack2(0.0f, 0.0f);
@@ -255,6 +300,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 dD = fmaf(dyss, v, dD);
                 const f32x2 dyss2 = pack2(dyss, dyss), dt2 = pack2(dt, dt), v2 = pack2(v, v);
                 const f32x2 one2 = pack2(1.0f, 1.0f);
+                const f32x2 dtsq2 = pack2(dt * dt, dt * dt);
                 f32x2 dvp = pack2(0.0f, 0.0f), ddtp = pack2(0.0f, 0.0f);
                 f32x2 red2[16];
 #pragma unroll
@@ -269,18 +315,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                         dEdt = one2;
                         dEda = pack2(0.0f, 0.0f);
                     } else {
-                        // exact forms (zoh_factor, zoh_factor_da): Taylor series where |dt a| < 2^-4, where
+                        // exact forms (zoh_factor2, zoh_factor_da2): Taylor series where |dt a| is small, where
                         // (Abar - 1) / a and (dt Abar - E) / a would cancel; the limits dt and dt^2 / 2 at a = 0
-                        float ab0, ab1, av0, av1, iv0, iv1, y0, y1;
-                        unpack2(Ab, ab0, ab1);
-                        unpack2(a2[p], av0, av1);
-                        unpack2(inva2[p], iv0, iv1);
-                        unpack2(y2, y0, y1);
-                        const float E0 = zoh_factor(dt, y0, ab0, iv0);
-                        const float E1 = zoh_factor(dt, y1, ab1, iv1);
-                        E = pack2(E0, E1);
+                        E = zoh_factor2(dt2, y2, Ab, ninv2[p]);
                         dEdt = Ab;
-                        dEda = pack2(zoh_factor_da(dt, dt * av0, ab0, E0, iv0), zoh_factor_da(dt, dt * av1, ab1, E1, iv1));
+                        dEda = zoh_factor_da2(dt2, dtsq2, mul2(dt2, a2[p]), Ab, E, inva2[p]);
                     }
                     const f32x2 dAb = mul2(g2[p], hprev[p]);
                     const f32x2 dBb = mul2(g2[p], v2);
@@ -331,10 +370,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
 #pragma unroll
                 for (int k = 0; k < 8; ++k) trow[k] = make_ulonglong2(red2[2 * k], red2[2 * k + 1]);
                 __syncwarp();
-                float sum = 0.0f;
+                // four independent partial sums: a 32-long chain of dependent adds would cost ~128 cycles
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int k = 0; k < 32; ++k) sum += sh.tr[warp][k][lane];
-                sh.ws[warp][j][lane] = sum;
+                for (int k = 0; k < 32; ++k) s4[k & 3] += sh.tr[warp][k][lane];
+                sh.ws[warp][j][lane] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 __syncwarp();
             }
             // outputs of the group
@@ -508,9 +548,11 @@ cudaError_t launch_bwd_z(const ScanBwdArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     dim3 grid(gx, (unsigned)a.Bsz, (unsigned)a.nseg);
-    if (a.conv_w) scan_bwd_kernel<Tin, NS, kZOH, true><<<grid, kBwdThreads, 0, s>>>(a);
-    else scan_bwd_kernel<Tin, NS, kZOH, false><<<grid, kBwdThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    auto kfn = a.conv_w ? scan_bwd_kernel<Tin, NS, kZOH, true> : scan_bwd_kernel<Tin, NS, kZOH, false>;
+    cudaError_t e = set_dynamic_smem_once(kfn, bwd_state_smem<NS>());
+    if (e != cudaSuccess) return e;
+    kfn<<<grid, kBwdThreads, bwd_state_smem<NS>(), s>>>(a);
+    e = cudaGetLastError();
     if (e != cudaSuccess || a.nseg <= 1 || !a.conv_w) return e;
     scan_bwd_boundary_kernel<Tin><<<dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), kBwdThreads, 0, s>>>(a);
     return cudaGetLastError();
@@ -543,11 +585,15 @@ const void* bwd_kernel_ptr_n(int N, int zoh, bool conv) {
     return bwd_kernel_ptr<Tin, 16>(zoh, conv);
 }
 
+int bwd_smem_n(int N) { return N <= 4 ? bwd_state_smem<4>() : N <= 8 ? bwd_state_smem<8>() : bwd_state_smem<16>(); }
+
 }  // namespace
 
 cudaError_t scan_bwd_resident_blocks(int dtype, int N, int zoh, bool conv, int* slots) {
     const void* k = dtype == 1 ? bwd_kernel_ptr_n<BF16>(N, zoh, conv) : bwd_kernel_ptr_n<F32>(N, zoh, conv);
-    return resident_blocks(k, kBwdThreads, 0, slots);
+    const cudaError_t e = set_dynamic_smem(k, bwd_smem_n(N));
+    if (e != cudaSuccess) return e;
+    return resident_blocks(k, kBwdThreads, bwd_smem_n(N), slots);
 }
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int dtype, int zoh, cudaStream_t stream) {

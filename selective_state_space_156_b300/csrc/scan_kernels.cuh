@@ -116,9 +116,10 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
             }
         }
         if (kFinal) out[j] = fmaf(cc.dskip, vj, y0 + y1) * gate[j];
-        if (kFinal && hall != nullptr) {
-            // the state after step tg + j: row (b, tg + j, d) of h_all, stride D * N per step
-            float* hp = hall + (size_t)(tg + j) * a.D * a.N;
+        if (kFinal && hall != nullptr && (a.hall_every <= 1 || j == 7 || tg + j == a.L - 1)) {
+            // the state after step tg + j: row (b, tg + j, d) of h_all, stride D * N per step; or, after a
+            // group's last step (tg is a multiple of 8), row (b, tg / 8, d) of the checkpoints
+            float* hp = hall + (size_t)(a.hall_every <= 1 ? tg + j : tg / 8) * a.D * a.N;
             if (a.N == NS && (reinterpret_cast<uintptr_t>(a.h_all) & 15) == 0) {  // whole rows: 16-byte stores
 #pragma unroll
                 for (int n = 0; n < NS; n += 4)
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_seq_kernel(const ScanKernel
     const int slot = a.state_indices != nullptr ? __ldg(a.state_indices + b) : b;
     const bool pad = slot < 0;
     const size_t srow = (size_t)(pad ? 0 : slot) * a.D + (active ? d : 0);
-    float* hall = (kFinal && a.h_all != nullptr && active && !pad) ? a.h_all + ((size_t)b * a.L * a.D + d) * a.N
+    const int hsteps = a.hall_every <= 1 ? a.L : (a.L + 7) / 8;  // rows of h_all per batch row
+    float* hall = (kFinal && a.h_all != nullptr && active && !pad) ? a.h_all + ((size_t)b * hsteps * a.D + d) * a.N
                                                                   : nullptr;
 
     ChannelConsts<NS> cc;

@@ -266,9 +266,10 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 #pragma unroll
             for (int p = 0; p < NSL / 2; ++p) acc = fma2(Cp[p], hp[p], acc);
         }
-        if (kHall && active) {
-            // the state after this step, into h_all (B, L, D, N): this lane's states, 16-byte stores
-            float* hp_out = hall + (size_t)(j0 + j) * a.D * a.N;
+        if (kHall && active && (a.hall_every <= 1 || j == 7)) {
+            // the state after this step, into h_all (B, L, D, N), or after the group's last step into the
+            // checkpoints (B, L / 8, D, N) (groups start at multiples of 8): this lane's states, 16-byte stores
+            float* hp_out = hall + (size_t)(a.hall_every <= 1 ? j0 + j : j0 / 8) * a.D * a.N;
             if (a.N == NS) {
 #pragma unroll
                 for (int p = 0; p < NSL / 2; p += 2)
@@ -464,8 +465,11 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
         const int clen = min(kP16Chunk, t_end - c0);
         // every lane of a warp takes part (the shuffles need them); inactive channels write nothing
         for (int j0 = 0; j0 < clen; j0 += 8) {
-            float* hall = kHall ? a.h_all + ((size_t)b * a.L * a.D + (active ? d : 0)) * a.N + e * NSL +
-                                          (size_t)c0 * a.D * a.N
+            // h_all: every step; checkpoints: every 8th (c0 is a multiple of 8)
+            const int hev = a.hall_every <= 1 ? 1 : 8;
+            const int hsteps = (a.L + hev - 1) / hev;
+            float* hall = kHall ? a.h_all + ((size_t)b * hsteps * a.D + (active ? d : 0)) * a.N + e * NSL +
+                                          (size_t)(c0 / hev) * a.D * a.N
                                 : nullptr;
             if (exact)
                 p16_group<NS, LPC, Disc::kZOHExact, kFinal, kConv, kHall>(a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum,

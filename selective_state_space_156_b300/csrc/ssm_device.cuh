@@ -189,6 +189,23 @@ __device__ __forceinline__ f32x2 zoh_factor2(f32x2 dt2, f32x2 y2, f32x2 ab2, f32
     return pack2(fabsf(y0) < kZohSeriesY ? s0 : b0, fabsf(y1) < kZohSeriesY ? s1 : b1);
 }
 
+// zoh_factor_da on a pair of states (the same series, coefficients and threshold): x2 = dt a, dt22 = dt^2,
+// E2 = zoh_factor2(...), inva2 = 1/a (0 where a == 0).
+__device__ __forceinline__ f32x2 zoh_factor_da2(f32x2 dt2, f32x2 dt22, f32x2 x2, f32x2 ab2, f32x2 E2, f32x2 inva2) {
+    const f32x2 big = mul2(fma2(dt2, ab2, mul2(E2, pack2(-1.0f, -1.0f))), inva2);  // one rounding, as fmaf
+    f32x2 p = fma2(x2, pack2(1.0f / 840.0f, 1.0f / 840.0f), pack2(1.0f / 144.0f, 1.0f / 144.0f));
+    p = fma2(p, x2, pack2(1.0f / 30.0f, 1.0f / 30.0f));
+    p = fma2(p, x2, pack2(0.125f, 0.125f));
+    p = fma2(p, x2, pack2(1.0f / 3.0f, 1.0f / 3.0f));
+    p = fma2(p, x2, pack2(0.5f, 0.5f));
+    const f32x2 small = mul2(dt22, p);
+    float x0, x1, s0, s1, b0, b1;
+    unpack2(x2, x0, x1);
+    unpack2(small, s0, s1);
+    unpack2(big, b0, b1);
+    return pack2(fabsf(x0) < kZohDaSeriesX ? s0 : b0, fabsf(x1) < kZohDaSeriesX ? s1 : b1);
+}
+
 // ---------------------------------------------------------------------------------------------
 // bf16 <-> fp32.  bf16 is the top half of an fp32, so widening is a shift; narrowing rounds to
 // nearest even with cvt.rn.bf16x2.f32.

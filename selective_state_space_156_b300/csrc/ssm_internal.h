@@ -27,7 +27,9 @@ struct ScanKernelArgs {
     int conv_width;
     const void* conv_init;  // (rows, conv_width - 1) x before t = 0 (in dtype), or NULL for zeros
     const int* state_indices;  // (B) slot of each batch row in h0 / h_out / conv_init, or NULL (slot = b)
-    float* h_all;              // (B, L, D, N) state after every step, or NULL
+    float* h_all;              // (B, ceil(L / hall_every), D, N): the state after every hall_every-th step
+                               // (entry c after step min(c hall_every + hall_every - 1, L - 1)), or NULL
+    int hall_every;            // 1 (h_all) or SSM_CKPT_STEPS (h_ckpt)
     const float* h0;
     float* h_out;
     void* y;
@@ -107,7 +109,7 @@ struct ScanBwdArgs {
     int conv_width;
     const void* conv_init;
     const float* h0;
-    const float* h_all;   // (B, L, D, N) the forward's state after every step
+    const float* h_ckpt;  // (B, ceil(L / 8), D, N) the forward's state after steps 7, 15, ... (and L - 1)
     const void* dy;
     const float* dh_out;  // (B, D, N) or NULL
     void* du;

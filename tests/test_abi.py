@@ -75,7 +75,7 @@ def test_params_struct_layout_matches_c():
     got = _c_layout("ssm_scan_params", """
   F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(out_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip)
   F(delta_bias) F(z) F(conv_w) F(conv_b) F(conv_width) F(h0) F(h_out) F(y) F(delta_softplus) F(zoh)
-  F(workspace) F(workspace_bytes) F(conv_init) F(conv_final) F(state_indices) F(h_all)""")
+  F(workspace) F(workspace_bytes) F(conv_init) F(conv_final) F(state_indices) F(h_all) F(h_ckpt)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanParams)
     assert len(got) == len(ssm.ScanParams._fields_)
     for name, off in got.items():
@@ -201,10 +201,23 @@ def test_scan_rejects_conv_final_overlapping_an_input(L):
     assert "conv_final overlaps" in L.ssm_last_error().decode()
 
 
+def test_scan_rejects_h_all_with_h_ckpt_and_overlapping_checkpoints(L):
+    p = _params(h_all=(1 << 40) + (9 << 30), h_ckpt=(1 << 40) + (12 << 30))
+    assert L.ssm_scan_fwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "alternatives" in L.ssm_last_error().decode()
+    p = _params(h_ckpt=(1 << 40) + 64)  # inside u
+    assert L.ssm_scan_fwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "h_ckpt overlaps" in L.ssm_last_error().decode()
+
+
+def test_checkpoint_count():
+    assert [ssm.ckpt_count(L) for L in (1, 7, 8, 9, 16, 2048, 2049)] == [1, 1, 1, 2, 2, 256, 257]
+
+
 def test_bwd_params_struct_layout_matches_c():
     got = _c_layout("ssm_scan_bwd_params", """
   F(batch) F(dim) F(dstate) F(seqlen) F(in_dtype) F(u) F(delta) F(A) F(Bm) F(Cm) F(Dskip) F(delta_bias) F(z)
-  F(conv_w) F(conv_b) F(conv_width) F(conv_init) F(h0) F(delta_softplus) F(zoh) F(h_all) F(dy) F(dh_out) F(du)
+  F(conv_w) F(conv_b) F(conv_width) F(conv_init) F(h0) F(delta_softplus) F(zoh) F(h_ckpt) F(dy) F(dh_out) F(du)
   F(ddelta) F(dz) F(dA) F(dB) F(dC) F(dDskip) F(ddelta_bias) F(dconv_w) F(dconv_b) F(dconv_init) F(dh0)
   F(workspace) F(workspace_bytes)""")
     assert int(got.pop("sizeof")) == ctypes.sizeof(ssm.ScanBwdParams)
@@ -217,7 +230,7 @@ def test_bwd_rejects_bad_arguments_on_host(L):
     p = ssm.ScanBwdParams()
     p.batch, p.dim, p.dstate, p.seqlen, p.in_dtype = 2, 64, 16, 128, ssm.SSM_BF16
     fake = 1 << 40
-    for i, k in enumerate(["u", "delta", "A", "Bm", "Cm", "h_all", "dy", "du", "ddelta", "dA", "dB", "dC"]):
+    for i, k in enumerate(["u", "delta", "A", "Bm", "Cm", "h_ckpt", "dy", "du", "ddelta", "dA", "dB", "dC"]):
         setattr(p, k, fake + (i << 32))
     p.delta_softplus, p.zoh = 1, 1
     p.dstate = 32

@@ -1,6 +1,7 @@
 """Parity of the backward pass (ssm_scan_bwd) against the fp64 autograd oracle, through the C ABI.
 
-The forward runs on the GPU with h_all (the state after every step), the backward consumes it; every
+The forward runs on the GPU keeping state checkpoints (h_ckpt, every 8th step), the backward recomputes
+the other states from them; every
 gradient is compared element by element with the oracle's on the same (rounded) inputs and dy.  Small
 problems cover the flags (conv with history, gate, zero-order hold or simplified, softplus on or off, an
 A = 0 entry, dh_out, h0), ragged L and a ragged channel tail; the Mamba-1.4B layer shape is checked on
@@ -9,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import selective_state_space_156_b300 as ssm
 import workloads
 from gpu_helpers import assert_close, to_dev
@@ -37,11 +39,11 @@ def _run(d, dy, dh_out=None, workspace="auto"):
     N = g["A"].shape[1]
     kw = dict(Dskip=g.get("Dskip"), delta_bias=g.get("delta_bias"), z=g.get("z"), conv_w=g.get("conv_w"),
               conv_b=g.get("conv_b"), delta_softplus=d.get("delta_softplus", True), zoh=d.get("zoh", True))
-    h_all = torch.empty((Bsz, L, D, N), dtype=torch.float32, device="cuda")
-    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g.get("h0"), h_all=h_all,
+    h_ckpt = torch.empty((Bsz, ssm.ckpt_count(L), D, N), dtype=torch.float32, device="cuda")
+    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g.get("h0"), h_ckpt=h_ckpt,
                      conv_init=g.get("conv_init"), **kw)
     dyd = dy.to(g["u"].dtype).cuda()
-    grads = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dyd, h_all, h0=g.get("h0"),
+    grads = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dyd, h_ckpt, h0=g.get("h0"),
                              conv_init=g.get("conv_init"), dh_out=None if dh_out is None else dh_out.cuda(),
                              workspace=workspace, **kw)
     torch.cuda.synchronize()
@@ -150,3 +152,26 @@ def test_backward_with_the_l_split_matches_oracle(dt, conv, L):
     for k, v in plain.items():
         tol = 2e-2 if v.dtype == torch.bfloat16 else 1e-4
         torch.testing.assert_close(grads[k].float(), v.float(), rtol=tol, atol=tol * float(v.float().abs().max() + 1e-6))
+
+
+@pytest.mark.parametrize("dt,L,D,split", [("bf16", 2048, 136, True), ("bf16", 512, 300, False),
+                                          ("f32", 1021, 70, True), ("f32", 77, 40, False)])
+def test_forward_checkpoints_are_the_states_at_every_8th_step(dt, L, D, split):
+    """h_ckpt from the forward (packed kernel for aligned bf16, element-wise kernel otherwise; with and
+    without the L split) holds the oracle's state after steps 7, 15, ... and after the last step."""
+    d = _inputs(2, D, 16, L, dt, 9900 + L, conv=(dt == "bf16"))
+    g = to_dev(d)
+    h_ckpt = torch.full((2, ssm.ckpt_count(L), D, 16), float("nan"), dtype=torch.float32, device="cuda")
+    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], Dskip=g.get("Dskip"),
+                     delta_bias=g.get("delta_bias"), z=g.get("z"), conv_w=g.get("conv_w"), conv_b=g.get("conv_b"),
+                     conv_init=g.get("conv_init"), h0=g.get("h0"), h_ckpt=h_ckpt,
+                     workspace="auto" if split else None)
+    torch.cuda.synchronize()
+    extra = {"h_all": True}
+    oracle.scan(d, extra=extra)
+    ha = extra["h_all"].reshape(2, D, L, 16)
+    steps = [min(8 * c + 7, L - 1) for c in range(ssm.ckpt_count(L))]
+    want = np.transpose(ha[:, :, steps, :], (0, 2, 1, 3))
+    got = h_ckpt.double().cpu().numpy()
+    tol = (1e-4 if dt == "f32" else 1e-3) * (1.0 + np.abs(want))
+    assert_close(got, want, tol, "h_ckpt")

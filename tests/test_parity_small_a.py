@@ -163,13 +163,13 @@ def test_backward(dt, dtype):
     g = to_dev(d)
     Bsz, D, L = g["u"].shape
     N = 16
-    h_all = torch.empty((Bsz, L, D, N), dtype=torch.float32, device="cuda")
+    h_ckpt = torch.empty((Bsz, ssm.ckpt_count(L), D, N), dtype=torch.float32, device="cuda")
     kw = dict(Dskip=g["Dskip"], z=g["z"], delta_softplus=False, zoh=True)
-    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g["h0"], h_all=h_all, **kw)
+    ssm.ssm_scan_fwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g["h0"], h_ckpt=h_ckpt, **kw)
     gen = torch.Generator().manual_seed(67)
     dy = torch.randn((Bsz, D, L), generator=gen).to(g["u"].dtype)
     dh = torch.randn((Bsz, D, N), generator=gen) * 0.3
-    grads = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dy.cuda(), h_all, h0=g["h0"],
+    grads = ssm.ssm_scan_bwd(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], dy.cuda(), h_ckpt, h0=g["h0"],
                              dh_out=dh.cuda(), **kw)
     torch.cuda.synchronize()
     ref = obwd.scan_bwd(d, dy.cpu(), dh)
