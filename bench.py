@@ -606,6 +606,17 @@ def run_other_configs(ssm, dev, skip: str, hbm_peak: float, fp32_peak: float, mu
                     ssm.ssm_scan_fwd(pc["u"], pc["delta"], g["A"], pc["Bm"], pc["Cm"], h0=h, h_out=h, y=yp,
                                      workspace=wsc, **dict(kw, z=pc["z"]))
             variants[f"{cfg.seqlen // cfg.chunk} chained calls"] = chained
+            # the same chain captured once as a CUDA graph: the calls' host work (argument checks, tensor
+            # maps, launches) leaves the timed path, as in a serving loop that replays a captured prefill
+            chained()
+            torch.cuda.synchronize()
+            cs = torch.cuda.Stream(device=dev)
+            cs.wait_stream(torch.cuda.current_stream())
+            gchain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gchain, stream=cs):
+                chained()
+            torch.cuda.current_stream().wait_stream(cs)
+            variants[f"{cfg.seqlen // cfg.chunk} chained calls, CUDA graph"] = gchain.replay
         res = {}
         for vname, fn in variants.items():
             for _ in range(3):

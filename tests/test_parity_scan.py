@@ -290,3 +290,46 @@ def test_g4_split_with_aliased_state(N):
     y, h = run_gpu(d, workspace="auto", alias_state=True)
     assert_close(y, y_ref.reshape(y.shape), y_tolerance(y_ref.reshape(y.shape), torch.bfloat16), "y")
     assert_close(h, h_ref.reshape(h.shape), h_tolerance(h_ref.reshape(h.shape), torch.bfloat16), "h_out")
+
+
+def test_chained_calls_captured_in_a_cuda_graph():
+    """A prefill in 8 chunked calls (carried state, L split through a preallocated workspace) captured once
+    as a CUDA graph and replayed: bit-identical to the same calls made directly, and within the bound of
+    the oracle."""
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["long2.8b"], batch=1, dim=256, seqlen=4096, with_h0=True)
+    g = to_dev(d)
+    pieces = [{k: g[k][..., a:a + 512].contiguous() for k in ("u", "delta", "z", "Bm", "Cm")}
+              for a in range(0, 4096, 512)]
+    kw = dict(Dskip=g["Dskip"], delta_bias=g["delta_bias"])
+    p0 = pieces[0]
+    ws = torch.empty(max(ssm.ssm_scan_workspace_size(p0["u"], p0["delta"], g["A"], p0["Bm"], p0["Cm"], h0=g["h0"],
+                                                     z=p0["z"], **kw), 1), dtype=torch.uint8, device="cuda")
+    h = torch.empty_like(g["h0"])
+    ys = [torch.empty_like(pc["u"]) for pc in pieces]
+
+    def chain():
+        h.copy_(g["h0"])
+        for pc, yc in zip(pieces, ys):
+            ssm.ssm_scan_fwd(pc["u"], pc["delta"], g["A"], pc["Bm"], pc["Cm"], z=pc["z"], h0=h, h_out=h, y=yc,
+                             workspace=ws, **kw)
+
+    chain()
+    torch.cuda.synchronize()
+    y_direct = torch.cat([y.clone() for y in ys], dim=-1)
+    h_direct = h.clone()
+    for y in ys:
+        y.zero_()
+    h.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(ys, dim=-1), y_direct)
+    assert torch.equal(h, h_direct)
+    y_ref, h_ref, _ = oracle.scan(d)
+    assert_close(y_direct, y_ref.reshape(y_direct.shape), y_tolerance(y_ref.reshape(y_direct.shape), torch.bfloat16), "y")
+    assert_close(h_direct, h_ref.reshape(h.shape), h_tolerance(h_ref.reshape(h.shape), torch.bfloat16), "h")
