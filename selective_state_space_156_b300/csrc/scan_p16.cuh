@@ -175,7 +175,7 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
             c = fmaf(w[1], xm2, c);
             c = fmaf(w[2], xm1, c);
             c = fmaf(w[3], xs[k], c);
-            v[k] = silu_fast(c);
+            v[k] = fmaf(c, tanh_mufu(c), c);  // SiLU(2c) = c + c tanh(c): the taps and bias are pre-halved
         }
     } else {
 #pragma unroll
@@ -189,10 +189,21 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 #pragma unroll
         for (int k = 0; k < SPL; k += 2) {
             const uint32_t dw = *reinterpret_cast<const uint32_t*>(drow + k);
-            const float s0 = bf16_lo(dw) + bias, s1 = bf16_hi(dw) + bias;
-            const float p0 = softplus_fast(s0), p1 = softplus_fast(s1);
-            dto[k] = sp_on ? p0 : s0;
-            dto[k + 1] = sp_on ? p1 : s1;
+            if (kDisc == Disc::kZOH) {
+                // the fast form needs the step only as the exponent argument dt a log2 e: keep it in base-2
+                // units, t = dt log2 e = max(s', 0) + log2(1 + 2^-|s'|) with s' = s log2 e (bias pre-scaled),
+                // and multiply by a (not a log2 e) below
+                const float s0 = fmaf(bf16_lo(dw), kLog2e, bias), s1 = fmaf(bf16_hi(dw), kLog2e, bias);
+                const float p0 = fmaxf(s0, 0.0f) + lg2_mufu(1.0f + ex2(-fabsf(s0)));
+                const float p1 = fmaxf(s1, 0.0f) + lg2_mufu(1.0f + ex2(-fabsf(s1)));
+                dto[k] = sp_on ? p0 : s0;
+                dto[k + 1] = sp_on ? p1 : s1;
+            } else {
+                const float s0 = bf16_lo(dw) + bias, s1 = bf16_hi(dw) + bias;
+                const float p0 = softplus_fast(s0), p1 = softplus_fast(s1);
+                dto[k] = sp_on ? p0 : s0;
+                dto[k + 1] = sp_on ? p1 : s1;
+            }
         }
     }
     if (kFinal) {
@@ -292,7 +303,7 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
             for (int m = 1; m < LPC; m <<= 1) y += __shfl_xor_sync(0xffffffffu, y, m);
             if (j / SPL == e) out[j % SPL] = y;
         } else {
-            dsum += dtj;
+            dsum += kDisc == Disc::kZOH ? dtj * kLn2 : dtj;  // the fast form's dtj is in base-2 units
         }
     }
     if (kFinal && active) {
@@ -385,6 +396,9 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
         w[2] = W >= 2 ? __ldg(cw + 2 - (4 - W)) : 0.0f;
         w[3] = __ldg(cw + 3 - (4 - W));
         if (a.conv_b != nullptr) cb = __ldg(a.conv_b + d);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] *= 0.5f;  // exact: the conv output enters SiLU as halves
+        cb *= 0.5f;
     }
     const float dskip = (a.Dskip != nullptr && active) ? __ldg(a.Dskip + d) : 0.0f;
     const float bias = (a.delta_bias != nullptr && active) ? __ldg(a.delta_bias + d) : 0.0f;
@@ -423,6 +437,21 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
 
     const bool exact = kZOH && __syncthreads_or(small_a);  // block-uniform choice of loop body
     const size_t yoff = row * (size_t)a.L;
+    // the fast form takes its step in base-2 units (see p16_group): A unscaled, the bias times log2 e
+    float bias_used = bias;
+    if (kZOH && !exact) {
+        bias_used = bias * kLog2e;
+#pragma unroll
+        for (int p = 0; p < NSL / 2; ++p) {
+            float av[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int n = e * NSL + 2 * p + q;
+                av[q] = (active && n < a.N) ? __ldg(a.A + (size_t)d * a.N + n) : 0.0f;
+            }
+            cc.al2[p] = pack2(av[0], av[1]);
+        }
+    }
 
     int buf = 0, k = 0;
     for (int c0 = t_begin; c0 < t_end; c0 += kP16Chunk, buf ^= 1, ++k) {
@@ -476,7 +505,7 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
                                                                           has_z, active, yoff + c0, hall);
             else
                 p16_group<NS, LPC, kZOH ? Disc::kZOH : Disc::kSimple, kFinal, kConv, kHall>(
-                    a, sm, buf, j0, cc, w, cb, dskip, bias, hp, dsum, has_z, active, yoff + c0, hall);
+                    a, sm, buf, j0, cc, w, cb, dskip, bias_used, hp, dsum, has_z, active, yoff + c0, hall);
         }
     }
 
