@@ -23,6 +23,7 @@
 // ssm_device_error reads and stops; before the block leaves, one thread waits (bounded) for the copies
 // it issued but did not consume.
 #include <algorithm>
+#include <type_traits>
 
 #include "bulk_copy.cuh"
 #include "ssm_device.cuh"
@@ -230,87 +231,105 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Cv[4 * c + i] = t4[i];
             }
-#pragma unroll
-            for (int p = 0; p < kTileRows / RPP; ++p) {
-                // every lane takes part in the shuffles; rows past the tile's end compute on stale values
-                // and store nothing
-                const int r = p * RPP + tid / TPR;
-                float h[SL], A4[SL];
-#pragma unroll
-                for (int c = 0; c < SL / 4; ++c) {
-                    const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + SL * q + 4 * c);
-                    const float4 av = *reinterpret_cast<const float4*>(As + r * N + SL * q + 4 * c);
-                    h[4 * c] = hv.x; h[4 * c + 1] = hv.y; h[4 * c + 2] = hv.z; h[4 * c + 3] = hv.w;
-                    A4[4 * c] = av.x; A4[4 * c + 1] = av.y; A4[4 * c + 2] = av.z; A4[4 * c + 3] = av.w;
-                }
-                // bf16 I/O: warps whose states all have |A| >= kZohFastMinA take the fast zero-order-hold
-                // form (its error is far inside the bf16 bound there); fp32 I/O always the exact form
+            // bf16 I/O: a warp whose rows in this tile all have |A| >= kZohFastMinA takes the fast zero-order-
+            // hold form (its error is far inside the bf16 bound there); fp32 I/O always the exact form.  One
+            // vote per tile and warp, and the row loop instantiated once per form: a per-row choice inside
+            // the unrolled loop measured 5 % slower than either form alone.
+            bool exact = T::kBytes != 2;
+            if (kZOH && !exact) {
                 bool small_a = false;
 #pragma unroll
-                for (int i = 0; i < SL; ++i) small_a |= !(fabsf(A4[i]) >= kZohFastMinA);
-                const bool exact = T::kBytes != 2 || __any_sync(0xffffffffu, small_a);
-                float uv = smem_scalar<T>(st + L::kOffU, r);
-                if constexpr (kConv) {
-                    // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}); x before t is the row's conv state
-                    const int W1 = a.W - 1;
-                    const float* cw = reinterpret_cast<const float*>(st + L::kOffCW) + r * a.W;
-                    float c = a.conv_b ? reinterpret_cast<const float*>(st + L::kOffCB)[r] : 0.0f;
+                for (int p = 0; p < kTileRows / RPP; ++p) {
+                    const int r = p * RPP + tid / TPR;  // rows past the tile's end hold stale values: harmless
 #pragma unroll
-                    for (int k = 0; k < 3; ++k)
-                        if (k < W1) c = fmaf(cw[k], smem_scalar<T>(st + L::kOffCS, r * W1 + k), c);
-                    c = fmaf(cw[W1], uv, c);
-                    if (q == 0 && r < rows) {
-                        // the new conv state: the last W - 1 inputs, oldest first (raw values, no rounding)
-                        using Sx = typename T::storage;
-                        const Sx* cs = reinterpret_cast<const Sx*>(st + L::kOffCS) + r * W1;
-                        Sx* out = static_cast<Sx*>(a.conv_state) + (s0 + r) * W1;
-#pragma unroll
-                        for (int k = 0; k < 3; ++k)
-                            if (k < W1) out[k] = k + 1 < W1 ? cs[k + 1] : reinterpret_cast<const Sx*>(st + L::kOffU)[r];
+                    for (int c = 0; c < SL / 4; ++c) {
+                        const float4 av = *reinterpret_cast<const float4*>(As + r * N + SL * q + 4 * c);
+                        small_a |= !(fabsf(av.x) >= kZohFastMinA) || !(fabsf(av.y) >= kZohFastMinA) ||
+                                   !(fabsf(av.z) >= kZohFastMinA) || !(fabsf(av.w) >= kZohFastMinA);
                     }
-                    if constexpr (T::kBytes == 2) uv = silu_fast(c);
-                    else uv = silu(c);
                 }
-                const float sr = smem_scalar<T>(st + L::kOffDt, r) + (a.delta_bias ? bs[r] : 0.0f);
-                const float zr = a.z ? smem_scalar<T>(st + L::kOffZ, r) : 0.0f;
-                const float dsk = a.Dskip ? Ds[r] : 0.0f;
-                float dt, gate;
-                if constexpr (T::kBytes == 2) {  // bf16 I/O: the MUFU forms
-                    dt = a.softplus ? softplus_fast(sr) : sr;
-                    gate = a.z ? silu_fast(zr) : 1.0f;
-                } else {
-                    dt = a.softplus ? softplus(sr) : sr;
-                    gate = a.z ? silu(zr) : 1.0f;
-                }
-                const float dtu = dt * uv;
-                float yp = 0.0f;
-#pragma unroll
-                for (int i = 0; i < SL; ++i) {
-                    const float y = dt * (A4[i] * kLog2e);
-                    const float ab = ex2(y);
-                    if (kZOH && exact) {
-                        // exact form, branch-free: E from the series where |dt a| < 2^-4 (dt at a = 0)
-                        const float E = zoh_factor(dt, y, ab, A4[i] != 0.0f ? rcp(A4[i]) : 0.0f);
-                        h[i] = fmaf(ab, h[i], E * (uv * Bv[i]));
-                    } else if (kZOH) {
-                        // fast form h' = Abar (h - ng) + ng, ng = -(v / a) B (every |a| >= 1/4 in the warp)
-                        const float ng = (uv * -rcp(A4[i])) * Bv[i];
-                        h[i] = fmaf(ab, h[i] - ng, ng);
-                    } else {
-                        h[i] = fmaf(ab, h[i], dtu * Bv[i]);
-                    }
-                    yp = fmaf(Cv[i], h[i], yp);
-                }
-#pragma unroll
-                for (int m = 1; m < TPR; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
-                if (r < rows) {
-#pragma unroll
-                    for (int c = 0; c < SL / 4; ++c)
-                        __stcs(reinterpret_cast<float4*>(a.state + (s0 + r) * N + SL * q + 4 * c),
-                               make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]));
-                    if (q == 0) store1<T>(a.y, r0 + r, fmaf(dsk, uv, yp) * gate);
-                }
+                exact = __any_sync(0xffffffffu, small_a);
             }
+            auto rows_pass = [&](auto exact_form) {
+                constexpr bool kExact = decltype(exact_form)::value;
+    #pragma unroll
+                for (int p = 0; p < kTileRows / RPP; ++p) {
+                    // every lane takes part in the shuffles; rows past the tile's end compute on stale values
+                    // and store nothing
+                    const int r = p * RPP + tid / TPR;
+                    float h[SL], A4[SL];
+    #pragma unroll
+                    for (int c = 0; c < SL / 4; ++c) {
+                        const float4 hv = *reinterpret_cast<const float4*>(hs + r * N + SL * q + 4 * c);
+                        const float4 av = *reinterpret_cast<const float4*>(As + r * N + SL * q + 4 * c);
+                        h[4 * c] = hv.x; h[4 * c + 1] = hv.y; h[4 * c + 2] = hv.z; h[4 * c + 3] = hv.w;
+                        A4[4 * c] = av.x; A4[4 * c + 1] = av.y; A4[4 * c + 2] = av.z; A4[4 * c + 3] = av.w;
+                    }
+                    float uv = smem_scalar<T>(st + L::kOffU, r);
+                    if constexpr (kConv) {
+                        // v = SiLU(conv_b + sum_k w_k x_{t-W+1+k}); x before t is the row's conv state
+                        const int W1 = a.W - 1;
+                        const float* cw = reinterpret_cast<const float*>(st + L::kOffCW) + r * a.W;
+                        float c = a.conv_b ? reinterpret_cast<const float*>(st + L::kOffCB)[r] : 0.0f;
+    #pragma unroll
+                        for (int k = 0; k < 3; ++k)
+                            if (k < W1) c = fmaf(cw[k], smem_scalar<T>(st + L::kOffCS, r * W1 + k), c);
+                        c = fmaf(cw[W1], uv, c);
+                        if (q == 0 && r < rows) {
+                            // the new conv state: the last W - 1 inputs, oldest first (raw values, no rounding)
+                            using Sx = typename T::storage;
+                            const Sx* cs = reinterpret_cast<const Sx*>(st + L::kOffCS) + r * W1;
+                            Sx* out = static_cast<Sx*>(a.conv_state) + (s0 + r) * W1;
+    #pragma unroll
+                            for (int k = 0; k < 3; ++k)
+                                if (k < W1) out[k] = k + 1 < W1 ? cs[k + 1] : reinterpret_cast<const Sx*>(st + L::kOffU)[r];
+                        }
+                        if constexpr (T::kBytes == 2) uv = silu_fast(c);
+                        else uv = silu(c);
+                    }
+                    const float sr = smem_scalar<T>(st + L::kOffDt, r) + (a.delta_bias ? bs[r] : 0.0f);
+                    const float zr = a.z ? smem_scalar<T>(st + L::kOffZ, r) : 0.0f;
+                    const float dsk = a.Dskip ? Ds[r] : 0.0f;
+                    float dt, gate;
+                    if constexpr (T::kBytes == 2) {  // bf16 I/O: the MUFU forms
+                        dt = a.softplus ? softplus_fast(sr) : sr;
+                        gate = a.z ? silu_fast(zr) : 1.0f;
+                    } else {
+                        dt = a.softplus ? softplus(sr) : sr;
+                        gate = a.z ? silu(zr) : 1.0f;
+                    }
+                    const float dtu = dt * uv;
+                    float yp = 0.0f;
+    #pragma unroll
+                    for (int i = 0; i < SL; ++i) {
+                        const float y = dt * (A4[i] * kLog2e);
+                        const float ab = ex2(y);
+                        if (kZOH && kExact) {
+                            // exact form, branch-free: E from the series where |dt a| < 2^-4 (dt at a = 0)
+                            const float E = zoh_factor(dt, y, ab, A4[i] != 0.0f ? rcp(A4[i]) : 0.0f);
+                            h[i] = fmaf(ab, h[i], E * (uv * Bv[i]));
+                        } else if (kZOH) {
+                            // fast form h' = Abar (h - ng) + ng, ng = -(v / a) B (every |a| >= 1/4 in the warp)
+                            const float ng = (uv * -rcp(A4[i])) * Bv[i];
+                            h[i] = fmaf(ab, h[i] - ng, ng);
+                        } else {
+                            h[i] = fmaf(ab, h[i], dtu * Bv[i]);
+                        }
+                        yp = fmaf(Cv[i], h[i], yp);
+                    }
+    #pragma unroll
+                    for (int m = 1; m < TPR; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
+                    if (r < rows) {
+    #pragma unroll
+                        for (int c = 0; c < SL / 4; ++c)
+                            __stcs(reinterpret_cast<float4*>(a.state + (s0 + r) * N + SL * q + 4 * c),
+                                   make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]));
+                        if (q == 0) store1<T>(a.y, r0 + r, fmaf(dsk, uv, yp) * gate);
+                    }
+                }
+            };
+            if (exact) rows_pass(std::true_type{});
+            else rows_pass(std::false_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
