@@ -35,9 +35,19 @@ constexpr int kBwdGroup = 8;    // steps per group (vector loads / stores, one r
 constexpr int kCkpt = SSM_CKPT_STEPS;  // steps per forward checkpoint: one group
 static_assert(kCkpt == kBwdGroup, "a group starts right after a checkpoint");
 
-// Dynamic shared memory of the backward kernel: the group's recomputed states.
+// Per-thread scalars of a group kept in shared memory for the reverse walk (a step loop that is not
+// unrolled would otherwise index register arrays at run time, which puts them in local memory, and with
+// two blocks' shared memory on the SM the L1 left over cannot hold that): per step dt, the softplus
+// argument s, the conv output c (the SSM input v without conv) and dy, z; then x_{tg-3} .. x_{tg+7}.
+enum BwdField { kFDt = 0, kFS, kFC, kFGy, kFZ, kFX };
+constexpr int kBwdScalars = kFX * kBwdGroup + kBwdGroup + 3;
+
+// Dynamic shared memory of the backward kernel: the group's recomputed states h_tg .. h_tg+6 (h_tg+7
+// stays in registers), then the scalars above.
 template <int NS>
-constexpr int bwd_state_smem() { return kBwdGroup * NS * kBwdThreads * (int)sizeof(float); }
+constexpr int bwd_state_smem() {
+    return ((kBwdGroup - 1) * NS + kBwdScalars) * kBwdThreads * (int)sizeof(float);
+}
 
 template <int NS>
 struct BwdShared {
@@ -51,6 +61,12 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + ex2(
 template <typename T>
 __device__ __forceinline__ float ld(const void* p, size_t i, bool ok) {
     return ok ? load1<T>(p, i) : 0.0f;
+}
+
+// Asks L2 for the line that holds element i of base; no register waits on it.
+template <typename T>
+__device__ __forceinline__ void prefetch_l2(const void* base, size_t i) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(base) + i * T::kBytes));
 }
 
 template <typename Tin, int NS, bool kZOH, bool kConv>
@@ -126,6 +142,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     // state before the group, h_{tg-1}, stays in registers.
     extern __shared__ float4 bwd_hs[];
     auto hs_at = [&](int j, int q) -> float4& { return bwd_hs[(j * (NS / 4) + q) * kBwdThreads + tid]; };
+    float* const bwd_sc = reinterpret_cast<float*>(bwd_hs + (kBwdGroup - 1) * (NS / 4) * kBwdThreads);
+    auto sc_at = [&](int f, int j) -> float& { return bwd_sc[(f * kBwdGroup + j) * kBwdThreads + tid]; };
     const int nck = (L + kCkpt - 1) / kCkpt;
     const float* crow = a.h_ckpt + ((size_t)b * nck * a.D + dd) * N;  // entry c: the state after step 8c + 7
     const size_t cstride = (size_t)a.D * N;
@@ -134,13 +152,34 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     for (int c0 = last_chunk; c0 >= t0; c0 -= kBwdChunk) {
         const int clen = min(kBwdChunk, t1 - c0);
         __syncthreads();  // everyone is done with the previous chunk's B / C
-        for (int i = tid; i < 2 * NS * kBwdChunk; i += kBwdThreads) {
-            const int wv = i / (NS * kBwdChunk);
-            const int rem = i - wv * NS * kBwdChunk;
-            const int n = rem / kBwdChunk, t = rem - n * kBwdChunk;
-            float val = 0.0f;
-            if (n < N && t < clen) val = load1<Tin>(wv ? a.Cm : a.Bm, ((size_t)b * N + n) * L + c0 + t);
-            sh.bc[wv][t][n] = val;
+        {
+            // all of a thread's loads first, then the stores (one memory latency per chunk)
+            constexpr int kStage = 2 * NS * kBwdChunk / kBwdThreads;
+            float stage[kStage];
+#pragma unroll
+            for (int r = 0; r < kStage; ++r) {
+                const int i = tid + r * kBwdThreads;
+                const int wv = i / (NS * kBwdChunk);
+                const int rem = i - wv * NS * kBwdChunk;
+                const int n = rem / kBwdChunk, t = rem - n * kBwdChunk;
+                stage[r] = (n < N && t < clen) ? load1<Tin>(wv ? a.Cm : a.Bm, ((size_t)b * N + n) * L + c0 + t) : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < kStage; ++r) {
+                const int i = tid + r * kBwdThreads;
+                const int wv = i / (NS * kBwdChunk);
+                const int rem = i - wv * NS * kBwdChunk;
+                const int n = rem / kBwdChunk, t = rem - n * kBwdChunk;
+                sh.bc[wv][t][n] = stage[r];
+            }
+        }
+        // the next chunk's B / C rows into L2 while this chunk runs
+        if (c0 - kBwdChunk >= t0 && tid < 2 * NS && tid % NS < N) {
+            const void* base = tid >= NS ? a.Cm : a.Bm;
+            const size_t o = ((size_t)b * N + tid % NS) * L + c0 - kBwdChunk;
+            prefetch_l2<Tin>(base, o);
+            prefetch_l2<Tin>(base, o + kBwdChunk / 2);
+            prefetch_l2<Tin>(base, o + kBwdChunk - 1);
         }
         __syncthreads();
         const int last_group = ((clen - 1) / kBwdGroup) * kBwdGroup;
@@ -168,6 +207,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     gy[j] = ld<Tin>(a.dy, rowoff + tg + j, ok);
                 }
             }
+            // the next group's rows (the eight steps before this one) and its checkpoint into L2 while
+            // this group runs
+            if (active && tg - kBwdGroup >= t0) {
+                const size_t o = rowoff + tg - kBwdGroup;
+                prefetch_l2<Tin>(a.u, o);
+                prefetch_l2<Tin>(a.delta, o);
+                if (has_z) prefetch_l2<Tin>(a.z, o);
+                prefetch_l2<Tin>(a.dy, o);
+                if (tg - kBwdGroup > 0) prefetch_l2<F32>(crow, (size_t)((tg - kBwdGroup) / kCkpt - 1) * cstride);
+            }
             if (kConv) {
                 const int W1 = a.conv_width - 1;
 #pragma unroll
@@ -178,11 +227,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     else if (active && a.conv_init && t >= -W1) xh[k] = load1<Tin>(a.conv_init, row * W1 + W1 + t);
                 }
             }
-            // per-step scalars of the group: SSM input v (conv pre-activation c), step dt
-            float vv[kBwdGroup], cv[kBwdGroup], sv[kBwdGroup], dtv[kBwdGroup];
+            // per-step scalars of the group: SSM input v (conv output c), step dt; kept for the reverse walk
+            float vv[kBwdGroup], dtv[kBwdGroup];
 #pragma unroll
             for (int j = 0; j < kBwdGroup; ++j) {
-                float c = 0.0f, v;
+                float v;
                 if (kConv) {
                     float xm[4];
 #pragma unroll
@@ -190,18 +239,29 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                         const int m = j - 3 + k;  // x_{t-3+k}
                         xm[k] = m >= 0 ? xv[m >= 0 ? m : 0] : xh[m + 3 >= 0 ? m + 3 : 0];
                     }
-                    c = fmaf(w[0], xm[0], cb);
+                    float c = fmaf(w[0], xm[0], cb);
                     c = fmaf(w[1], xm[1], c);
                     c = fmaf(w[2], xm[2], c);
                     c = fmaf(w[3], xm[3], c);
-                    v = silu(c);
+                    v = c * sigmoid_f(c);  // SiLU, formed as the reverse walk forms it
+                    sc_at(kFC, j) = c;
                 } else {
                     v = xv[j];
+                    sc_at(kFC, j) = v;
                 }
-                cv[j] = c;
                 vv[j] = v;
-                sv[j] = dv[j] + bias;
-                dtv[j] = a.softplus ? softplus(sv[j]) : sv[j];
+                const float sj = dv[j] + bias;
+                dtv[j] = a.softplus ? softplus(sj) : sj;
+                sc_at(kFDt, j) = dtv[j];
+                sc_at(kFS, j) = sj;
+                sc_at(kFGy, j) = gy[j];
+                sc_at(kFZ, j) = zv[j];
+            }
+            if (kConv) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) sc_at(kFX, k) = xh[k];
+#pragma unroll
+                for (int j = 0; j < kBwdGroup; ++j) sc_at(kFX, 3 + j) = xv[j];
             }
             // the state before the group (the previous group's checkpoint, or h0), then the group's states
             // recomputed forward from it with the forward pass's zero-order hold (exact form)
@@ -242,6 +302,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                         if (kZOH) E = zoh_factor2(dt2, y2, Ab, ninv2[p]);
                         hcur[p] = fma2(Ab, hcur[p], mul2(E, mul2(v2, Bt[p])));
                     }
+                    if (j == kBwdGroup - 1) break;  // the group's last state stays in hcur
 #pragma unroll
                     for (int k = 0; k < NS / 4; ++k) {
                         float h0_, h1_, h2_, h3_;
@@ -251,23 +312,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     }
                 }
             }
-            float du_o[kBwdGroup], dd_o[kBwdGroup], dz_o[kBwdGroup];
             // not unrolled: the step body is large (eight state pairs), and eight copies of it overflow the
-            // instruction cache (4.86 -> 4.48 ms on the 8 x 4096 x 16 x 2048 layer); the per-step arrays
-            // indexed by j live in local memory (L1)
+            // instruction cache (4.86 -> 4.48 ms on the 8 x 4096 x 16 x 2048 layer); the per-step scalars
+            // come from shared memory, and the step's input gradients go back into its dt, s and z slots
 #pragma unroll 1
             for (int j = kBwdGroup - 1; j >= 0; --j) {
-                du_o[j] = dd_o[j] = dz_o[j] = 0.0f;
                 if (j >= nv) continue;  // uniform over the block: nv is
                 const int t = tg + j;
-                const float v = vv[j], c = cv[j], s = sv[j], dt = dtv[j];
+                const float dt = sc_at(kFDt, j), s = sc_at(kFS, j), gyj = sc_at(kFGy, j), zj = sc_at(kFZ, j);
+                float c = 0.0f, sgc = 0.0f, v;
+                if (kConv) {
+                    c = sc_at(kFC, j);
+                    sgc = sigmoid_f(c);
+                    v = c * sgc;
+                } else {
+                    v = sc_at(kFC, j);
+                }
                 float xm[4];
                 if (kConv) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int m = j - 3 + k;  // x_{t-3+k}
-                        xm[k] = m >= 0 ? xv[m >= 0 ? m : 0] : xh[m + 3 >= 0 ? m + 3 : 0];
-                    }
+                    for (int k = 0; k < 4; ++k) xm[k] = sc_at(kFX, j + k);  // x_{t-3+k}
                 }
                 // h_t (in hcur since the previous step, or from the forward recompute) and h_{t-1}
                 f32x2 hprev[NS / 2];
@@ -290,12 +354,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 float ya, yb;
                 unpack2(yacc, ya, yb);
                 const float yss = fmaf(dsk, v, ya + yb);
-                float dyss = gy[j];
+                float dyss = gyj;
                 if (has_z) {
-                    const float sg = sigmoid_f(zv[j]);
-                    const float gz = zv[j] * sg;
-                    dz_o[j] = gy[j] * yss * sg * (1.0f + zv[j] * (1.0f - sg));
-                    dyss = gy[j] * gz;
+                    const float sg = sigmoid_f(zj);
+                    const float gz = zj * sg;
+                    sc_at(kFZ, j) = gyj * yss * sg * (1.0f + zj * (1.0f - sg));  // dz
+                    dyss = gyj * gz;
                 }
                 dD = fmaf(dyss, v, dD);
                 const f32x2 dyss2 = pack2(dyss, dyss), dt2 = pack2(dt, dt), v2 = pack2(v, v);
@@ -341,23 +405,22 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 const float ddt = d0 + d1;
                 const float ds = a.softplus ? ddt * sigmoid_f(s) : ddt;
                 dbias += ds;
-                dd_o[j] = ds;
+                sc_at(kFS, j) = ds;  // d delta
                 if (kConv) {
-                    const float sc = sigmoid_f(c);
-                    const float dc = dvv * sc * (1.0f + c * (1.0f - sc));
+                    const float dc = dvv * sgc * (1.0f + c * (1.0f - sgc));
                     dcb += dc;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         dw[k] = fmaf(dc, xm[k], dw[k]);
                         px[3 - k] = fmaf(dc, w[k], px[3 - k]);     // x_{t-3+k} is pending slot 3 - k
                     }
-                    du_o[j] = px[0];
+                    sc_at(kFDt, j) = px[0];  // du
                     px[0] = px[1];
                     px[1] = px[2];
                     px[2] = px[3];
                     px[3] = 0.0f;
                 } else {
-                    du_o[j] = dvv;
+                    sc_at(kFDt, j) = dvv;  // du
                 }
                 // the warp's sum of each of the 32 values (dB n, dC n): every lane writes its row of 32
                 // with 16-byte stores, every lane then sums one column (rows padded to 36 floats: both
@@ -378,6 +441,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 __syncwarp();
             }
             // outputs of the group
+            float du_o[kBwdGroup], dd_o[kBwdGroup], dz_o[kBwdGroup];
+#pragma unroll
+            for (int j = 0; j < kBwdGroup; ++j) {
+                du_o[j] = sc_at(kFDt, j);
+                dd_o[j] = sc_at(kFS, j);
+                dz_o[j] = sc_at(kFZ, j);
+            }
             if (active && a.vec && nv == kBwdGroup) {
                 store8<Tin>(a.du, rowoff + tg, du_o);
                 store8<Tin>(a.ddelta, rowoff + tg, dd_o);
