@@ -207,6 +207,31 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     gy[j] = ld<Tin>(a.dy, rowoff + tg + j, ok);
                 }
             }
+            // the state before the group (the previous group's checkpoint, or h0), loaded with the inputs so
+            // that the two latencies overlap
+            f32x2 hstart[NS / 2];
+            {
+                const float* src = tg > 0 ? crow + (size_t)(tg / kCkpt - 1) * cstride : a.h0 ? a.h0 + row * N : nullptr;
+                // src is NULL before t = 0 without h0: the state is zero, nothing is read
+                const bool vec4 = src != nullptr && (N == NS) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+                if (vec4 && active) {
+                    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(src);
+#pragma unroll
+                    for (int k = 0; k < NS / 4; ++k) {
+                        const ulonglong2 w2 = __ldcs(q + k);
+                        hstart[2 * k] = w2.x;
+                        hstart[2 * k + 1] = w2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        float hv[2];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) hv[q] = (src && active && 2 * p + q < N) ? src[2 * p + q] : 0.0f;
+                        hstart[p] = pack2(hv[0], hv[1]);
+                    }
+                }
+            }
             // the next group's rows (the eight steps before this one) and its checkpoint into L2 while
             // this group runs
             if (active && tg - kBwdGroup >= t0) {
@@ -263,30 +288,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
 #pragma unroll
                 for (int j = 0; j < kBwdGroup; ++j) sc_at(kFX, 3 + j) = xv[j];
             }
-            // the state before the group (the previous group's checkpoint, or h0), then the group's states
-            // recomputed forward from it with the forward pass's zero-order hold (exact form)
-            f32x2 hstart[NS / 2], hcur[NS / 2];
+            // the group's states recomputed forward from the state before it with the forward pass's
+            // zero-order hold (exact form)
+            f32x2 hcur[NS / 2];
             {
-                const float* src = tg > 0 ? crow + (size_t)(tg / kCkpt - 1) * cstride : a.h0 ? a.h0 + row * N : nullptr;
-                // src is NULL before t = 0 without h0: the state is zero, nothing is read
-                const bool vec4 = src != nullptr && (N == NS) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
-                if (vec4 && active) {
-                    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(src);
-#pragma unroll
-                    for (int k = 0; k < NS / 4; ++k) {
-                        const ulonglong2 w2 = __ldcs(q + k);
-                        hstart[2 * k] = w2.x;
-                        hstart[2 * k + 1] = w2.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int p = 0; p < NS / 2; ++p) {
-                        float hv[2];
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) hv[q] = (src && active && 2 * p + q < N) ? src[2 * p + q] : 0.0f;
-                        hstart[p] = pack2(hv[0], hv[1]);
-                    }
-                }
 #pragma unroll
                 for (int p = 0; p < NS / 2; ++p) hcur[p] = hstart[p];
 #pragma unroll
