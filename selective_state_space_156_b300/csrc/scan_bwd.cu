@@ -63,6 +63,21 @@ __device__ __forceinline__ float ld(const void* p, size_t i, bool ok) {
     return ok ? load1<T>(p, i) : 0.0f;
 }
 
+// zoh_factor2 given 1/a instead of -1/a ((Abar - 1)(1/a) is (1 - Abar)(-1/a) exactly): the kernel keeps one
+// reciprocal per state in registers, not two.
+__device__ __forceinline__ f32x2 zoh_e2(f32x2 dt2, f32x2 y2, f32x2 ab2, f32x2 inva2) {
+    f32x2 p = fma2(y2, pack2(kPhiY3, kPhiY3), pack2(kPhiY2, kPhiY2));
+    p = fma2(p, y2, pack2(kPhiY1, kPhiY1));
+    p = fma2(p, y2, pack2(1.0f, 1.0f));
+    const f32x2 small = mul2(p, dt2);
+    const f32x2 big = mul2(sub2(ab2, pack2(1.0f, 1.0f)), inva2);
+    float y0, y1, s0, s1, b0, b1;
+    unpack2(y2, y0, y1);
+    unpack2(small, s0, s1);
+    unpack2(big, b0, b1);
+    return pack2(fabsf(y0) < kZohSeriesY ? s0 : b0, fabsf(y1) < kZohSeriesY ? s1 : b1);
+}
+
 // Asks L2 for the line that holds element i of base; no register waits on it.
 template <typename T>
 __device__ __forceinline__ void prefetch_l2(const void* base, size_t i) {
@@ -85,7 +100,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     const int t1 = min(L, t0 + a.seg_len);
 
     // per-channel constants, as packed pairs of states (n, n + 1)
-    f32x2 a2[NS / 2], al2[NS / 2], inva2[NS / 2], ninv2[NS / 2];
+    // (the exponent argument dt a log2 e is formed as (dt log2 e) a, one scalar product per step)
+    f32x2 a2[NS / 2], inva2[NS / 2];
 #pragma unroll
     for (int p = 0; p < NS / 2; ++p) {
         float av[2], iv[2];
@@ -96,9 +112,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
             iv[q] = av[q] != 0.0f ? 1.0f / av[q] : 0.0f;
         }
         a2[p] = pack2(av[0], av[1]);
-        al2[p] = pack2(av[0] * kLog2e, av[1] * kLog2e);
         inva2[p] = pack2(iv[0], iv[1]);
-        ninv2[p] = pack2(-iv[0], -iv[1]);
     }
     float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
     if (kConv && active) {
@@ -131,7 +145,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
             float gv[2];
 #pragma unroll
             for (int q = 0; q < 2; ++q) gv[q] = (active && 2 * p + q < N) ? gl[2 * p + q] : 0.0f;
-            g2[p] = fma2(ex2x2(mul2(pack2(S, S), al2[p])), g2[p], pack2(gv[0], gv[1]));
+            g2[p] = fma2(ex2x2(mul2(pack2(S * kLog2e, S * kLog2e), a2[p])), g2[p], pack2(gv[0], gv[1]));
         }
     }
     float dD = 0.0f, dbias = 0.0f, dw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dcb = 0.0f;
@@ -299,12 +313,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     if (j >= nv) break;  // uniform over the block
                     const f32x2* Bt = reinterpret_cast<const f32x2*>(sh.bc[0][tg + j - c0]);
                     const f32x2 dt2 = pack2(dtv[j], dtv[j]), v2 = pack2(vv[j], vv[j]);
+                    const float dtl = dtv[j] * kLog2e;
+                    const f32x2 dtl2 = pack2(dtl, dtl);
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p) {
-                        const f32x2 y2 = mul2(dt2, al2[p]);
+                        const f32x2 y2 = mul2(dtl2, a2[p]);
                         const f32x2 Ab = ex2x2(y2);
                         f32x2 E = dt2;
-                        if (kZOH) E = zoh_factor2(dt2, y2, Ab, ninv2[p]);
+                        if (kZOH) E = zoh_e2(dt2, y2, Ab, inva2[p]);
                         hcur[p] = fma2(Ab, hcur[p], mul2(E, mul2(v2, Bt[p])));
                     }
                     if (j == kBwdGroup - 1) break;  // the group's last state stays in hcur
@@ -370,13 +386,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                 const f32x2 dyss2 = pack2(dyss, dyss), dt2 = pack2(dt, dt), v2 = pack2(v, v);
                 const f32x2 one2 = pack2(1.0f, 1.0f);
                 const f32x2 dtsq2 = pack2(dt * dt, dt * dt);
+                const float dtl = dt * kLog2e;
+                const f32x2 dtl2 = pack2(dtl, dtl);
                 f32x2 dvp = pack2(0.0f, 0.0f), ddtp = pack2(0.0f, 0.0f);
                 f32x2 red2[16];
 #pragma unroll
                 for (int p = 0; p < NS / 2; ++p) {
                     g2[p] = fma2(Ct[p], dyss2, g2[p]);
                     red2[8 + p] = mul2(dyss2, hcur[p]);                 // dC contribution
-                    const f32x2 y2 = mul2(dt2, al2[p]);
+                    const f32x2 y2 = mul2(dtl2, a2[p]);
                     const f32x2 Ab = ex2x2(y2);
                     f32x2 E, dEdt, dEda;
                     if (!kZOH) {
@@ -386,7 +404,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     } else {
                         // exact forms (zoh_factor2, zoh_factor_da2): Taylor series where |dt a| is small, where
                         // (Abar - 1) / a and (dt Abar - E) / a would cancel; the limits dt and dt^2 / 2 at a = 0
-                        E = zoh_factor2(dt2, y2, Ab, ninv2[p]);
+                        E = zoh_e2(dt2, y2, Ab, inva2[p]);
                         dEdt = Ab;
                         dEda = zoh_factor_da2(dt2, dtsq2, mul2(dt2, a2[p]), Ab, E, inva2[p]);
                     }
