@@ -117,7 +117,11 @@ SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
     if (want > maxseg) want = maxseg;
     if (want > 64) want = 64;
     if (want <= 1) return p;
-    const int seg = (int)(((L + want - 1) / want + chunk - 1) / chunk) * chunk;
+    // the packed kernel needs segment starts on 8-step boundaries only (16-byte staged rows, 8-step groups
+    // and checkpoints), so its segments are as even as that allows (2048 steps in 7: 6 x 296 + 272, not
+    // 6 x 336 + 32 with 48-step chunks); the other kernels cut at their chunk length
+    const int align = kind == ssm::kScanP16 ? 8 : chunk;
+    const int seg = (int)(((L + want - 1) / want + align - 1) / align) * align;
     p.seg_len = seg;
     p.nseg = (L + seg - 1) / seg;
     return p;
