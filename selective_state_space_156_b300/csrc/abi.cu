@@ -103,7 +103,13 @@ int choose_lpc(const ssm_scan_params* p) {
 struct SegPlan {
     int nseg;
     int seg_len;
+    int seg0_len;  // > 0: segment 0 has this length and runs its final pass beside the summaries
 };
+
+// A summary pass costs about this much of a final pass per step (percent; measured on the 1 x 5120 x 16
+// x 65536 workload: 1.16 of 2.86 ms against 1.70): segment 0, whose final pass runs beside the summaries,
+// is this much shorter than the others so that both end together.
+constexpr int kSummaryCostPct = 68;
 
 SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
     const KindGeom kg = kind_geom(kind, lpc);
@@ -117,11 +123,26 @@ SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
     if (want > maxseg) want = maxseg;
     if (want > 64) want = 64;
     if (want <= 1) return p;
-    // the packed kernel needs segment starts on 8-step boundaries only (16-byte staged rows, 8-step groups
-    // and checkpoints), so its segments are as even as that allows (2048 steps in 7: 6 x 296 + 272, not
-    // 6 x 336 + 32 with 48-step chunks); the other kernels cut at their chunk length
-    const int align = kind == ssm::kScanP16 ? 8 : chunk;
-    const int seg = (int)(((L + want - 1) / want + align - 1) / align) * align;
+    if (kind == ssm::kScanP16) {
+        // Segment 0 needs no carry, so its final pass runs in the first launch beside the summaries of
+        // segments 1 .. want - 1, and its end state is the first carry; the second launch runs the final
+        // passes of segments 1 .. want.  That is want + 1 segments at want blocks per channel block in each
+        // launch.  Segment starts need 8-step boundaries only (16-byte staged rows, 8-step groups and
+        // checkpoints); segment 0 is shorter by the summary's cost.
+        long long ls = ((100LL * L + 100LL * want + kSummaryCostPct - 1) / (100LL * want + kSummaryCostPct) + 7) / 8 * 8;
+        long long l0 = L - want * ls;
+        while (l0 < 8 && ls > 8) {
+            ls -= 8;
+            l0 = L - want * ls;
+        }
+        if (l0 >= 8) {
+            p.nseg = (int)want + 1;
+            p.seg_len = (int)ls;
+            p.seg0_len = (int)l0;
+            return p;
+        }
+    }
+    const int seg = (int)(((L + want - 1) / want + chunk - 1) / chunk) * chunk;
     p.seg_len = seg;
     p.nseg = (L + seg - 1) / seg;
     return p;
@@ -498,6 +519,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, ssm_stream_t stream) {
     }
     a.nseg = sp.nseg;
     a.seg_len = sp.seg_len;
+    a.seg0_len = sp.seg0_len;
     if (sp.nseg > 1) {
         uintptr_t base = (reinterpret_cast<uintptr_t>(p->workspace) + 255) & ~(uintptr_t)255;
         const size_t rows = (size_t)p->batch * p->dim;
@@ -619,9 +641,11 @@ ssm_status ssm_scan_fwd_static(const ssm_scan_params* p, ssm_stream_t stream) {
                     need, kStaticScratchBytes);
     a.nseg = sp.nseg;
     a.seg_len = sp.seg_len;
+    a.seg0_len = sp.seg0_len;
     if (sp.nseg > 1) {
-        // Nothing here has to start at zero: the summary pass of this call writes every word of the
-        // scratch that its final pass reads (segment sums, segment end states, the copy of h0).
+        // Nothing here has to start at zero: the first launch of this call writes every word of the
+        // scratch that its final pass reads (segment sums, segment end states, the copy of h0 where it is
+        // used).
         void* base = nullptr;
         st = static_scratch_address(&base);
         if (st != SSM_OK) return st;

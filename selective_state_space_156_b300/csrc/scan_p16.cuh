@@ -323,9 +323,10 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 // Resident blocks per SM the register budget aims at, by lanes per channel.
 __host__ __device__ constexpr int p16_min_blocks(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
 
-template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false, bool kTma = false>
-__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
-    scan_p16_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
+// One block's pass over segment `seg` of its (batch row, channel block): the final pass (outputs) or the
+// summary pass (end state from a zero start and the sum of dt, for the L split).
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall, bool kTma>
+__device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& maps, const int seg) {
     constexpr int NSL = NS / LPC;
     constexpr int kCh = P16Smem<NS, LPC>::kCh;
     constexpr int kBcOff = kTma ? kP16Halo : 0;  // column of the chunk's first step in the staged B / C rows
@@ -334,14 +335,16 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
     uint64_t* tma_bar = sm.bar;
     const int tid = threadIdx.x;
     const int e = tid & (LPC - 1);
-    const int b = blockIdx.y, seg = blockIdx.z;
+    const int b = blockIdx.y;
     const int ch0 = blockIdx.x * kCh;
     const int d = ch0 + tid / LPC;
     const bool active = d < a.D;
     const size_t rows = (size_t)a.Bsz * a.D;
     const size_t row = (size_t)b * a.D + (active ? d : 0);
-    const int t_begin = seg * a.seg_len;
-    const int t_end = min(a.L, t_begin + a.seg_len);
+    // segments: [s seg_len, (s + 1) seg_len), or with a first segment of seg0_len steps, [0, seg0_len) and
+    // then seg_len steps each
+    const int t_begin = a.seg0_len > 0 ? (seg == 0 ? 0 : a.seg0_len + (seg - 1) * a.seg_len) : seg * a.seg_len;
+    const int t_end = min(a.L, (a.seg0_len > 0 && seg == 0) ? a.seg0_len : t_begin + a.seg_len);
     const bool has_z = kFinal && a.z != nullptr;
 
     // B/C rows past N stay zero (cp.async never writes them)
@@ -410,13 +413,25 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
     for (int i = 0; i < NSL; ++i) h[i] = 0.0f;
     float dsum = 0.0f;
     if (kFinal) {
-        const float* h0 = (a.nseg > 1) ? a.ws_h0 : a.h0;
-        if (h0 != nullptr && active) {
+        // the state at the segment's start: h0 (its copy when the summaries ran first), or with a first
+        // segment the end state of segment 0 from the first launch; then the later summaries folded in
+        int s_first = 0;
+        if (a.seg0_len > 0 && seg > 0) {
+            if (active) {
 #pragma unroll
-            for (int i = 0; i < NSL; ++i)
-                if (n0 + i < a.N) h[i] = h0[row * a.N + n0 + i];
+                for (int i = 0; i < NSL; ++i)
+                    if (n0 + i < a.N) h[i] = a.ws_h[row * a.N + n0 + i];
+            }
+            s_first = 1;
+        } else {
+            const float* h0 = (a.nseg > 1 && a.seg0_len == 0) ? a.ws_h0 : a.h0;
+            if (h0 != nullptr && active) {
+#pragma unroll
+                for (int i = 0; i < NSL; ++i)
+                    if (n0 + i < a.N) h[i] = h0[row * a.N + n0 + i];
+            }
         }
-        for (int s = 0; s < seg; ++s) {
+        for (int s = s_first; s < seg; ++s) {
             const float S = active ? a.ws_dsum[(size_t)s * rows + row] : 0.0f;
 #pragma unroll
             for (int i = 0; i < NSL; ++i) {
@@ -518,12 +533,37 @@ __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
             for (int i = 0; i < NSL; ++i)
                 if (n0 + i < a.N) a.h_out[row * a.N + n0 + i] = h[i];
         }
+        if (seg == 0 && a.seg0_len > 0) {  // the first carry of the L split
+#pragma unroll
+            for (int i = 0; i < NSL; ++i)
+                if (n0 + i < a.N) a.ws_h[row * a.N + n0 + i] = h[i];
+        }
     } else {
         if (e == 0) a.ws_dsum[(size_t)seg * rows + row] = dsum;
 #pragma unroll
         for (int i = 0; i < NSL; ++i)
             if (n0 + i < a.N) a.ws_h[((size_t)seg * rows + row) * a.N + n0 + i] = h[i];
     }
+}
+
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false, bool kTma = false>
+__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
+    scan_p16_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
+    // with a first segment (seg0_len > 0) the first launch has run segment 0's final pass: this final
+    // pass covers segments 1 .. nseg - 1
+    p16_run<NS, LPC, kZOH, kFinal, kConv, kHall, kTma>(a, maps, (int)blockIdx.z + ((kFinal && a.seg0_len > 0) ? 1 : 0));
+}
+
+// The first launch of an L split with a first segment: block z = 0 runs segment 0's final pass (from h0;
+// its end state becomes the first carry, and it needs no summary), blocks z >= 1 the summaries of
+// segments 1 .. nseg - 2, at the same time.
+template <int NS, int LPC, bool kZOH, bool kConv, bool kHall, bool kTma>
+__global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
+    scan_p16_first_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
+    if (blockIdx.z == 0)
+        p16_run<NS, LPC, kZOH, true, kConv, kHall, kTma>(a, maps, 0);
+    else
+        p16_run<NS, LPC, kZOH, false, kConv, false, kTma>(a, maps, (int)blockIdx.z);
 }
 
 // SSM_SCAN_STAGING=cpasync stages chunks with per-thread cp.async copies instead of the tiled bulk copies
@@ -557,7 +597,11 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
     const unsigned gx = (unsigned)((a.D + kCh - 1) / kCh);
     cudaError_t e;
     if (a.nseg > 1) {
-        auto kfn = scan_p16_kernel<NS, LPC, kZOH, false, kConv, false, kTma>;
+        // the summaries of segments 0 .. nseg - 2, or with a first segment segment 0's final pass and the
+        // summaries of segments 1 .. nseg - 2
+        auto kfn = a.seg0_len > 0 ? (a.h_all != nullptr ? scan_p16_first_kernel<NS, LPC, kZOH, kConv, true, kTma>
+                                                        : scan_p16_first_kernel<NS, LPC, kZOH, kConv, false, kTma>)
+                                  : scan_p16_kernel<NS, LPC, kZOH, false, kConv, false, kTma>;
         e = set_dynamic_smem_once(kfn, (int)smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(kfn, dim3(gx, (unsigned)a.Bsz, (unsigned)(a.nseg - 1)), block, smem, stream, a, maps);
@@ -571,7 +615,8 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
     if (e != cudaSuccess) return e;
     ScanKernelArgs fa = a;
     fa.withhold = (kTma && a.nseg == 1 && withhold_first_copy()) ? 1 : 0;
-    e = launch_pdl(kfn, dim3(gx, (unsigned)a.Bsz, (unsigned)a.nseg), block, smem, stream, fa, maps);
+    const unsigned gz = (unsigned)(a.seg0_len > 0 ? a.nseg - 1 : a.nseg);
+    e = launch_pdl(kfn, dim3(gx, (unsigned)a.Bsz, gz), block, smem, stream, fa, maps);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

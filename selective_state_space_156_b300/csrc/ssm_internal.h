@@ -36,8 +36,11 @@ struct ScanKernelArgs {
     int softplus;
     int vec;       // 1: every (b, d) row of u/delta/z/y starts 16-byte aligned and L % 8 == 0
     int nseg;      // number of L segments (1 = one pass, no workspace)
-    int seg_len;   // timesteps per segment, a multiple of the chunk length; last one may be shorter
-    float* ws_h;     // (nseg - 1, B*D, N) end state of each segment but the last, from a zero start
+    int seg_len;   // timesteps per segment (a multiple of 8); the last one may be shorter
+    int seg0_len;  // kScanP16: > 0 when segment 0 has its own length (then [0, seg0_len), and seg_len steps
+                   // per later segment) and runs its final pass in the split's first launch; 0 otherwise
+    float* ws_h;     // (nseg - 1, B*D, N) end state of each segment but the last, from a zero start (with
+                     // seg0_len > 0, entry 0 is segment 0's end state from h0)
     float* ws_dsum;  // (nseg - 1, B*D) sum of dt over each segment but the last
     float* ws_h0;    // (B*D, N) copy of h0 taken before any block may write h_out (h0 may alias h_out)
     int kind;        // kScanSeq, kScanP16 or kScanG4
