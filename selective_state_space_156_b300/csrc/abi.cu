@@ -434,7 +434,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, ssm_stream_t stream) {
     const char* who = "ssm_scan_bwd";
     ssm_status vs = validate_bwd(p);
     if (vs != SSM_OK) return vs;
-    const size_t rows = (size_t)p->batch * p->dim, nbdl = rows * p->seqlen;
+    const size_t rows = (size_t)p->batch * p->dim;
     const size_t eb = esize(p->in_dtype);
     const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
     struct Range { const void* p; size_t n; };

@@ -324,8 +324,10 @@ __device__ __forceinline__ void p16_group(const ScanKernelArgs& a, const P16Smem
 __host__ __device__ constexpr int p16_min_blocks(int lpc) { return lpc == 1 ? 2 : (lpc == 2 ? 4 : 7); }
 
 // One block's pass over segment `seg` of its (batch row, channel block): the final pass (outputs) or the
-// summary pass (end state from a zero start and the sum of dt, for the L split).
-template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall, bool kTma>
+// summary pass (end state from a zero start and the sum of dt, for the L split).  kSeg0: the split has a
+// first segment of its own length (a.seg0_len) whose final pass runs in the first launch; else the
+// segments are [s seg_len, (s + 1) seg_len) (one of them when the sequence runs in one pass).
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall, bool kTma, bool kSeg0>
 __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& maps, const int seg) {
     constexpr int NSL = NS / LPC;
     constexpr int kCh = P16Smem<NS, LPC>::kCh;
@@ -343,8 +345,8 @@ __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& 
     const size_t row = (size_t)b * a.D + (active ? d : 0);
     // segments: [s seg_len, (s + 1) seg_len), or with a first segment of seg0_len steps, [0, seg0_len) and
     // then seg_len steps each
-    const int t_begin = a.seg0_len > 0 ? (seg == 0 ? 0 : a.seg0_len + (seg - 1) * a.seg_len) : seg * a.seg_len;
-    const int t_end = min(a.L, (a.seg0_len > 0 && seg == 0) ? a.seg0_len : t_begin + a.seg_len);
+    const int t_begin = kSeg0 ? (seg == 0 ? 0 : a.seg0_len + (seg - 1) * a.seg_len) : seg * a.seg_len;
+    const int t_end = min(a.L, (kSeg0 && seg == 0) ? a.seg0_len : t_begin + a.seg_len);
     const bool has_z = kFinal && a.z != nullptr;
 
     // B/C rows past N stay zero (cp.async never writes them)
@@ -416,7 +418,7 @@ __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& 
         // the state at the segment's start: h0 (its copy when the summaries ran first), or with a first
         // segment the end state of segment 0 from the first launch; then the later summaries folded in
         int s_first = 0;
-        if (a.seg0_len > 0 && seg > 0) {
+        if (kSeg0 && seg > 0) {
             if (active) {
 #pragma unroll
                 for (int i = 0; i < NSL; ++i)
@@ -424,7 +426,7 @@ __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& 
             }
             s_first = 1;
         } else {
-            const float* h0 = (a.nseg > 1 && a.seg0_len == 0) ? a.ws_h0 : a.h0;
+            const float* h0 = (!kSeg0 && a.nseg > 1) ? a.ws_h0 : a.h0;
             if (h0 != nullptr && active) {
 #pragma unroll
                 for (int i = 0; i < NSL; ++i)
@@ -533,7 +535,7 @@ __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& 
             for (int i = 0; i < NSL; ++i)
                 if (n0 + i < a.N) a.h_out[row * a.N + n0 + i] = h[i];
         }
-        if (seg == 0 && a.seg0_len > 0) {  // the first carry of the L split
+        if (kSeg0 && seg == 0) {  // the first carry of the L split
 #pragma unroll
             for (int i = 0; i < NSL; ++i)
                 if (n0 + i < a.N) a.ws_h[row * a.N + n0 + i] = h[i];
@@ -546,12 +548,13 @@ __device__ __forceinline__ void p16_run(const ScanKernelArgs& a, const P16Maps& 
     }
 }
 
-template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false, bool kTma = false>
+template <int NS, int LPC, bool kZOH, bool kFinal, bool kConv, bool kHall = false, bool kTma = false,
+          bool kSeg0 = false>
 __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
     scan_p16_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
-    // with a first segment (seg0_len > 0) the first launch has run segment 0's final pass: this final
-    // pass covers segments 1 .. nseg - 1
-    p16_run<NS, LPC, kZOH, kFinal, kConv, kHall, kTma>(a, maps, (int)blockIdx.z + ((kFinal && a.seg0_len > 0) ? 1 : 0));
+    // with a first segment (kSeg0) the first launch has run segment 0's final pass: this final pass covers
+    // segments 1 .. nseg - 1
+    p16_run<NS, LPC, kZOH, kFinal, kConv, kHall, kTma, kSeg0>(a, maps, (int)blockIdx.z + ((kFinal && kSeg0) ? 1 : 0));
 }
 
 // The first launch of an L split with a first segment: block z = 0 runs segment 0's final pass (from h0;
@@ -561,9 +564,9 @@ template <int NS, int LPC, bool kZOH, bool kConv, bool kHall, bool kTma>
 __global__ void __launch_bounds__(kP16Threads, p16_min_blocks(LPC))
     scan_p16_first_kernel(const ScanKernelArgs a, const __grid_constant__ P16Maps maps) {
     if (blockIdx.z == 0)
-        p16_run<NS, LPC, kZOH, true, kConv, kHall, kTma>(a, maps, 0);
+        p16_run<NS, LPC, kZOH, true, kConv, kHall, kTma, true>(a, maps, 0);
     else
-        p16_run<NS, LPC, kZOH, false, kConv, false, kTma>(a, maps, (int)blockIdx.z);
+        p16_run<NS, LPC, kZOH, false, kConv, false, kTma, true>(a, maps, (int)blockIdx.z);
 }
 
 // SSM_SCAN_STAGING=cpasync stages chunks with per-thread cp.async copies instead of the tiled bulk copies
@@ -609,8 +612,10 @@ cudaError_t launch_p16_staged(const ScanKernelArgs& a, const P16Maps& maps, cuda
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    auto kfn = a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true, kTma>
-                                  : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma>;
+    auto kfn = a.seg0_len > 0 ? (a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true, kTma, true>
+                                                    : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma, true>)
+                              : (a.h_all != nullptr ? scan_p16_kernel<NS, LPC, kZOH, true, kConv, true, kTma>
+                                                    : scan_p16_kernel<NS, LPC, kZOH, true, kConv, false, kTma>);
     e = set_dynamic_smem_once(kfn, (int)smem);
     if (e != cudaSuccess) return e;
     ScanKernelArgs fa = a;
