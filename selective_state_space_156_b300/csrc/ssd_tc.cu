@@ -7,27 +7,29 @@
 // a_t = exp(dt_t A) and s_i = sum_{t0 <= j <= i} dt_j A (log2 units in the code), per chunk:
 //
 //   [G | C S]  = C [B ; S^T]^T                    (Q x (Q + P) over the N states)        tensor cores
-//   M          = G o [j <= i] exp(s_i - s_j) w_j  + Dskip I                              threads -> smem
+//   M          = G o [j <= i] exp(s_i - s_j) w_j  + Dskip I                              threads -> TMEM
 //   Y          = exp(s_i) (C S) + M X              (inter-chunk + intra-chunk + skip)    tensor cores
 //   S         <- exp(s_end) S + B^T (v o X)^T,    v_j = exp(s_end - s_j) w_j             tensor cores
 //   y          = Y * SiLU(z)
 //
 // where w_j = dt_j (simplified input scale) or expm1(dt_j A) / A (zero-order hold).  C, B (Q x N) and X
 // (the head's P channels over the chunk) arrive by TMA in the 128-byte swizzle layout; the increment reads
-// B as it landed, as an MN-major operand.  The operands the threads build (M, v o X, S^T) are written in
-// the same layout as two bf16 terms, hi = bf16(u) and lo = bf16(u - hi), and every product with them is
-// issued for both terms into one accumulator, so their rounding costs about 2^-16 relative instead of
-// 2^-8.  S^T's two terms sit right below B in the same K blocks, which makes G and C S one N = 256
-// product per K step.
+// B as it landed, as an MN-major operand.  The operands the threads build (M, v o X, S^T) carry two bf16
+// terms, hi = bf16(u) and lo = bf16(u - hi), and every product with them is issued for both terms into
+// one accumulator, so their rounding costs about 2^-16 relative instead of 2^-8.  v o X and S^T are
+// written to shared memory in the copies' layout; S^T's two terms sit right below B in the same K blocks,
+// which makes G and C S one N = 256 product per K step.  M goes back into tensor memory over the G block
+// it was built from (16 fp32 columns of G hold the 8 + 8 columns of M's two terms) and is the A operand
+// of M X from there: it never passes through shared memory.
 //
-// Accumulators in TMEM: G in columns 0..127, C S_hi in 128..191, C S_lo in 192..255, M X in 256..319 and
-// the state increment in 320..383.  A dedicated warp issues the copies and the products; four compute
+// Accumulators in TMEM: G (then M) in columns 0..127, C S_hi in 128..191, C S_lo in 192..255, M X in
+// 256..319 and the state increment in 320..383.  A dedicated warp issues the copies and the products; four compute
 // warpgroups split the element-wise work (each warp reads the TMEM lanes of its quarter of the rows).
 // Overlaps within a chunk: the increment is issued as soon as v o X is built and runs while the threads
 // build M; it completes on a barrier of its own, so that the state update runs while M X is still on the
 // tensor cores.  Across chunks: the next chunk's C is fetched as soon as this chunk's first product is
-// done, its B, X and dt as soon as M X and the increment are; y leaves through a TMA store of the tile
-// staged in M's place.
+// done, its B, X and dt as soon as M X and the increment are; y leaves through a TMA store of a staged
+// tile.  Every product's shared-memory descriptors are built once; a K step adds a constant.
 #include <cstdint>
 
 #include "bulk_copy.cuh"
@@ -60,10 +62,8 @@ constexpr int kRowStHi = 128, kRowStLo = 192;    //   S^T lo (p x n)
 constexpr int kOffX = kOffBS + 2 * kBS;          // X: P rows (p) x Q (t), K blocks of 8 KB
 constexpr int kOffXs = kOffX + 2 * 8192;         // v o X hi, the same shape
 constexpr int kOffXsLo = kOffXs + 2 * 8192;      // v o X lo
-constexpr int kOffM = kOffXsLo + 2 * 8192;       // M hi: Q rows (i) x Q (j), K blocks of 16 KB; then the
-                                                 //   y tile (p x t, K blocks of 8 KB)
-constexpr int kOffMlo = kOffM + 2 * 16384;       // M lo
-constexpr int kOffS2 = kOffMlo + 2 * 16384;      // float s[Q]: cumulative log2 decay
+constexpr int kOffY = kOffXsLo + 2 * 8192;       // the y tile: P rows (p) x Q (t), K blocks of 8 KB
+constexpr int kOffS2 = kOffY + 2 * 8192;         // float s[Q]: cumulative log2 decay
 constexpr int kOffW = kOffS2 + kQ * 4;           // float w[Q]: input scale
 constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j) w_j
 constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
@@ -237,7 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t sC = smem_u32(sm + kOffC), sBS = smem_u32(sm + kOffBS), sX = smem_u32(sm + kOffX);
     const uint32_t sXs = smem_u32(sm + kOffXs), sXsLo = smem_u32(sm + kOffXsLo);
-    const uint32_t sM = smem_u32(sm + kOffM), sMlo = smem_u32(sm + kOffMlo);
+
+    // the operands' shared-memory descriptors, built once: a K step only moves the start address, which is
+    // the descriptor's low field (address / 16), so each product adds a constant to a base descriptor
+    const uint64_t dC = tc::desc_k_sw128(sC), dBS = tc::desc_k_sw128(sBS), dX = tc::desc_k_sw128(sX);
+    const uint64_t dXs = tc::desc_k_sw128(sXs), dXsLo = tc::desc_k_sw128(sXsLo);
+    const uint64_t dBmn = tc::desc_mn_sw128(sBS, kBS, 1024);
 
     unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
     // the issuer's view of its asynchronous work: issued and not yet seen complete by its own wait, with
@@ -261,15 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
                 const uint32_t kb = (ks >> 2) * kBS + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColG, tc::desc_k_sw128(sC + ka), tc::desc_k_sw128(sBS + kb), tc::idesc_bf16(128, 256),
-                             ks > 0);
+                tc::mma_bf16(tmem + kColG, dC + (ka >> 4), dBS + (kb >> 4), tc::idesc_bf16(128, 256), ks > 0);
             }
             tc::mma_commit(mma_bar);
             mma_pend = true;
             mma_par = 0;   // the first of the chunk's two commits
         }
         if (issuer) {
-            bulk_wait_read_all();   // the previous chunk's y store has left the M tile
+            bulk_wait_read_all();   // the previous chunk's y store has left the y tile (before its next writes)
         } else if (!issuer_warp) {
             // meanwhile: step sizes and the cumulative decay of the chunk, by warpgroup 0 (steps past L:
             // dt = 0, so a = 1 and w = 0)
@@ -332,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
                 const int k = ks & 7;
-                const uint32_t ka = sBS + k * 2048;   // 16 steps (rows t) of B per K step
-                const uint32_t kb = (ks < 8 ? sXs : sXsLo) + (k >> 2) * 8192 + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColSc, tc::desc_mn_sw128(ka, kBS, 1024), tc::desc_k_sw128(kb),
+                const uint32_t ka = k * 2048;   // 16 steps (rows t) of B per K step
+                const uint32_t kb = (k >> 2) * 8192 + (k & 3) * 32;
+                tc::mma_bf16(tmem + kColSc, dBmn + (ka >> 4), (ks < 8 ? dXs : dXsLo) + (kb >> 4),
                              tc::idesc_bf16(128, kP, true), ks > 0);
             }
             tc::mma_commit(inc_bar);
@@ -353,9 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float gv[16];
                 const bool live = 32 * quarter + 31 >= jb;   // warp-uniform: some row of this warp reaches jb
                 if (live) tc::tmem_ld16(tmem + tlane + kColG + jb, gv);
+                // the block's 16 columns of M as bf16 pairs: hi terms, then lo terms, written over the G block
+                // just read (its 16 fp32 columns hold 8 columns of each), the A operand of M X
+                uint32_t hi8[8], lo8[8];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+                    uint32_t* hi = hi8 + 4 * q;
+                    uint32_t* lo = lo8 + 4 * q;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hi[e] = lo[e] = 0u;
                     const int j0 = jb + q * 8;
                     if (live && j0 <= r) {
 #pragma unroll
@@ -375,25 +385,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             split_pair(v0, v1, hi[e], lo[e]);
                         }
                     }
-                    const uint32_t o = swz(16384, r, j0);
-                    st_shared_v4(sm + kOffM + o, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(sm + kOffMlo + o, lo[0], lo[1], lo[2], lo[3]);
                 }
+                tc::tmem_st8(tmem + tlane + kColG + jb, hi8);
+                tc::tmem_st8(tmem + tlane + kColG + jb + 8, lo8);
             }
+            tc::tmem_wait_st();
         }
-        tc::fence_async_smem();   // M and v o X
+        tc::fence_async_smem();   // v o X
         tc::fence_before();
         __syncthreads();
 
         if (issuer && !*abort_flag) {
-            // M X (both terms of M); the commit also covers the increment issued before it
+            // M X (both terms of M, A from tensor memory); the commit also covers the increment issued before it
             tc::fence_after();
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
                 const int k = ks & 7;
-                const uint32_t ka = (ks < 8 ? sM : sMlo) + (k >> 2) * 16384 + (k & 3) * 32;
-                const uint32_t kb = sX + (k >> 2) * 8192 + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColY2, tc::desc_k_sw128(ka), tc::desc_k_sw128(kb), tc::idesc_bf16(128, kP), ks > 0);
+                const uint32_t ta = tmem + kColG + 16 * k + (ks < 8 ? 0u : 8u);
+                const uint32_t kb = (k >> 2) * 8192 + (k & 3) * 32;
+                tc::mma_bf16_ts(tmem + kColY2, ta, dX + (kb >> 4), tc::idesc_bf16(128, kP), ks > 0);
             }
             tc::mma_commit(mma_bar);
             mma_pend = true;
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!issuer_warp) {
             // outputs of row i = r (step t), this warpgroup's channels: C S (both terms) and M X from TMEM,
-            // y staged as the y tile in M's place
+            // y staged as the y tile
             const int t = t0 + r;
             const float ei = ex2(s2_row);
 #pragma unroll
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 16; e += 2) {
                     float f, s2v;
                     pair_rows(y1[e], y1[e + 1], odd, f, s2v);
-                    st_shared_u32(sm + kOffM + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s2v));
+                    st_shared_u32(sm + kOffY + swz(8192, pb + e + odd, r & ~1), pack_bf16x2(f, s2v));
                 }
             }
         }
@@ -467,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before();
         __syncthreads();          // every TMEM and shared read of this chunk is done
         if (issuer && !*abort_flag) {
-            tma_store_2d(&map_y, t0, static_cast<int>(row0), sm + kOffM);
-            if (t0 + 64 < L) tma_store_2d(&map_y, t0 + 64, static_cast<int>(row0), sm + kOffM + 8192);
+            tma_store_2d(&map_y, t0, static_cast<int>(row0), sm + kOffY);
+            if (t0 + 64 < L) tma_store_2d(&map_y, t0 + 64, static_cast<int>(row0), sm + kOffY + 8192);
             bulk_commit_group();
         }
     }
