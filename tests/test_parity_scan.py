@@ -162,6 +162,28 @@ def test_split_path_is_taken_and_matches():
     torch.testing.assert_close(h_split, h_one, rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("dim,L", [(64, 512), (64, 1000), (200, 2048), (300, 4104), (40, 8192)])
+def test_split_segment_plans(dim, L):
+    """The packed kernel's L split at several grid sizes and lengths, so that the planner takes different
+    segment counts and first-segment lengths (segment 0's final pass runs beside the later segments'
+    summaries): every element against the oracle, with h0 and the gate."""
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba130m"], batch=1, dim=dim, seqlen=L, with_h0=True,
+                                   seed=4200 + dim + L)
+    g = to_dev(d)
+    assert ssm.ssm_scan_workspace_size(g["u"], g["delta"], g["A"], g["Bm"], g["Cm"], h0=g["h0"], z=g["z"]) > 0
+    check_full(d, workspace="auto")
+
+
+def test_packed_split_with_h0_aliasing_h_out():
+    """bf16 on the packed kernel with the L split and h0 == h_out: segment 0 reads h0 in the first launch,
+    the last segment writes h_out in the second."""
+    d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["mamba130m"], batch=1, dim=96, seqlen=4096, with_h0=True)
+    y_ref, h_ref, _ = oracle.scan(d)
+    y, h = run_gpu(d, workspace="auto", alias_state=True)
+    assert_close(y, y_ref.reshape(y.shape), y_tolerance(y_ref.reshape(y.shape), torch.bfloat16), "y")
+    assert_close(h, h_ref.reshape(h.shape), h_tolerance(h_ref.reshape(h.shape), torch.bfloat16), "h_out")
+
+
 def test_chained_calls_equal_one_call():
     d = workloads.make_scan_inputs(workloads.SCAN_CONFIGS["long2.8b"], batch=1, dim=64, seqlen=4096, with_h0=True)
     g = to_dev(d)
