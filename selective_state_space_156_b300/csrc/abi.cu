@@ -106,10 +106,11 @@ struct SegPlan {
     int seg0_len;  // > 0: segment 0 has this length and runs its final pass beside the summaries
 };
 
-// A summary pass costs about this much of a final pass per step (percent; measured on the 1 x 5120 x 16
-// x 65536 workload: 1.16 of 2.86 ms against 1.70): segment 0, whose final pass runs beside the summaries,
-// is this much shorter than the others so that both end together.
-constexpr int kSummaryCostPct = 68;
+// A summary launch costs about this much of a final launch per step (percent; ncu on 2048-step calls on
+// 5120 channels: 48.2 us for 272-step summaries against 60.4 us for 272-step final passes): segment 0,
+// whose final pass runs beside the summaries, is this much shorter than the others so that both end
+// together.
+constexpr int kSummaryCostPct = 80;
 
 SegPlan plan_segments(int kind, int lpc, int Bsz, int D, int L) {
     const KindGeom kg = kind_geom(kind, lpc);
