@@ -17,18 +17,19 @@
 // B as it landed, as an MN-major operand.  The operands the threads build (M, v o X, S^T) carry two bf16
 // terms, hi = bf16(u) and lo = bf16(u - hi), and every product with them is issued for both terms into
 // one accumulator, so their rounding costs about 2^-16 relative instead of 2^-8.  v o X and S^T are
-// written to shared memory in the copies' layout; S^T's two terms sit right below B in the same K blocks,
-// which makes G and C S one N = 256 product per K step.  M goes back into tensor memory over the G block
+// written to shared memory in the copies' layout; S^T's two terms sit right below B in the same K blocks
+// (one N = 128 product per K step for each of G and C S).  M goes back into tensor memory over the G block
 // it was built from (16 fp32 columns of G hold the 8 + 8 columns of M's two terms) and is the A operand
 // of M X from there: it never passes through shared memory.
 //
 // Accumulators in TMEM: G (then M) in columns 0..127, C S_hi in 128..191, C S_lo in 192..255, M X in
 // 256..319 and the state increment in 320..383.  A dedicated warp issues the copies and the products; four compute
 // warpgroups split the element-wise work (each warp reads the TMEM lanes of its quarter of the rows).
-// Overlaps within a chunk: the increment is issued as soon as v o X is built and runs while the threads
-// build M; it completes on a barrier of its own, so that the state update runs while M X is still on the
-// tensor cores.  Across chunks: the next chunk's C is fetched as soon as this chunk's first product is
-// done, its B, X and dt as soon as M X and the increment are; y leaves through a TMA store of a staged
+// Overlaps within a chunk: G is issued first and completes on its own, so that the M build starts while
+// C S is still on the tensor cores; the increment is issued as soon as v o X is built and runs while the
+// threads build M; it completes on a barrier of its own, so that the state update runs while M X is still
+// on the tensor cores.  Across chunks: the next chunk's C is fetched as soon as this chunk's C S is done,
+// its B, X and dt as soon as M X and the increment are; y leaves through a TMA store of a staged
 // tile.  Every product's shared-memory descriptors are built once; a K step adds a constant.
 #include <cstdint>
 
@@ -69,8 +70,8 @@ constexpr int kOffV = kOffW + kQ * 4;            // float v[Q]: exp2(s_end - s_j
 constexpr int kOffWarp = kOffV + kQ * 4;         // float[4]: warp totals of the prefix sum
 constexpr int kOffDt = kOffWarp + 16;            // bf16 dt[Q] of the chunk, copied with B and X
 constexpr int kOffBar = kOffDt + kQ * 2;         // uint64 barriers: C landed, B and X landed, products
-                                                 //   done, increment done
-constexpr int kOffTmem = kOffBar + 32;           // uint32 TMEM base, int abort flag
+                                                 //   done, increment done, C S done
+constexpr int kOffTmem = kOffBar + 48;           // uint32 TMEM base, int abort flag
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;     // slack for aligning the base
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar_bx = bar_c + 1;
     uint64_t* mma_bar = bar_c + 2;
     uint64_t* inc_bar = bar_c + 3;   // the chunk's state increment is done
+    uint64_t* cs_bar = bar_c + 4;    // the chunk's C S is done (C may be overwritten)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffTmem + 4);
     float* s2s = reinterpret_cast<float*>(sm + kOffS2);
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_bx, 1);
         mbar_init(mma_bar, 1);
         mbar_init(inc_bar, 1);
+        mbar_init(cs_bar, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_c);
         tma_prefetch_map(&map_b);
@@ -247,30 +250,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned c_phase = 0, bx_phase = 0, mma_phase = 0;
     // the issuer's view of its asynchronous work: issued and not yet seen complete by its own wait, with
     // the parity of the phase that completes it (a chunk's copies: the chunk's; products: their order)
-    bool c_pend = c_pend_init, bx_pend = true, mma_pend = false, inc_pend = false;
-    unsigned c_par = 0, bx_par = 0, mma_par = 0, inc_par = 0;
+    // one bit per barrier (C, B X, products, increment, C S) in `pend`, and the awaited parity in `par`
+    enum : unsigned { kPC = 1u, kPBX = 2u, kPMMA = 4u, kPINC = 8u, kPCS = 16u };
+    unsigned pend = (c_pend_init ? kPC : 0u) | kPBX, par = 0u;
+    auto set_pend = [&](unsigned bit, unsigned parity) { pend |= bit; par = parity ? (par | bit) : (par & ~bit); };
     const int nchunks = (L + kQ - 1) / kQ;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
         // this chunk's C, B, X and dt (issued a phase ahead); each thread waits for itself
-        if (wait_own(bar_c, c_phase, abort_flag)) c_pend = false;
-        if (wait_own(bar_bx, bx_phase, abort_flag)) bx_pend = false;
+        if (wait_own(bar_c, c_phase, abort_flag)) pend &= ~kPC;
+        if (wait_own(bar_bx, bx_phase, abort_flag)) pend &= ~kPBX;
         c_phase ^= 1u;
         bx_phase ^= 1u;
 
         float s2_end = 0.0f, s2_row = 0.0f;
         if (issuer && !*abort_flag) {
-            // [G | C S_hi | C S_lo] = C [B ; S^T hi ; S^T lo]^T: eight N = 256 products
+            // G = C B^T first (the M build waits for it alone), then [C S_hi | C S_lo] = C [S^T hi ; S^T lo]^T,
+            // which runs under the M build: eight N = 128 products each
             tc::fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
                 const uint32_t kb = (ks >> 2) * kBS + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColG, dC + (ka >> 4), dBS + (kb >> 4), tc::idesc_bf16(128, 256), ks > 0);
+                tc::mma_bf16(tmem + kColG, dC + (ka >> 4), dBS + (kb >> 4), tc::idesc_bf16(128, 128), ks > 0);
             }
             tc::mma_commit(mma_bar);
-            mma_pend = true;
-            mma_par = 0;   // the first of the chunk's two commits
+            set_pend(kPMMA, 0u);   // the first of the chunk's two commits
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint32_t kb = (ks >> 2) * kBS + kRowStHi * 128 + (ks & 3) * 32;
+                tc::mma_bf16(tmem + kColY1, dC + (ka >> 4), dBS + (kb >> 4), tc::idesc_bf16(128, 128), ks > 0);
+            }
+            tc::mma_commit(cs_bar);
+            set_pend(kPCS, c & 1);
         }
         if (issuer) {
             bulk_wait_read_all();   // the previous chunk's y store has left the y tile (before its next writes)
@@ -321,17 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_async_smem();   // v o X, read by the increment issued after the next barrier
         }
-        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) mma_pend = false;
+        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) pend &= ~kPMMA;
         mma_phase ^= 1u;
         tc::fence_before();
         __syncthreads();   // v o X is complete (and G is read by the M build behind this)
         tc::fence_after();
         if (issuer && !*abort_flag) {
-            if (c + 1 < nchunks) {   // C is free: the next chunk's copy overlaps the rest of this one
-                issue_c(c + 1);
-                c_pend = true;
-                c_par = (c + 1) & 1;
-            }
             // the increment B^T (v o X)^T (both terms of v o X), B read MN-major, under the M build
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
@@ -342,8 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              tc::idesc_bf16(128, kP, true), ks > 0);
             }
             tc::mma_commit(inc_bar);
-            inc_pend = true;
-            inc_par = c & 1;
+            set_pend(kPINC, c & 1);
+            // C is free once C S is done: the next chunk's copy overlaps the rest of this one
+            if (wait_own(cs_bar, c & 1, abort_flag)) pend &= ~kPCS;
+            if (c + 1 < nchunks && !*abort_flag) {
+                issue_c(c + 1);
+                set_pend(kPC, (c + 1) & 1);
+            }
         }
 
         // row i = r of M from row i of G, in 16-column blocks dealt round-robin to the warpgroups; blocks
@@ -406,12 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_bf16_ts(tmem + kColY2, ta, dX + (kb >> 4), tc::idesc_bf16(128, kP), ks > 0);
             }
             tc::mma_commit(mma_bar);
-            mma_pend = true;
-            mma_par = 1;   // the second
+            set_pend(kPMMA, 1u);   // the second
         }
         // the state first, while M X runs: S <- exp2(s_end) S + increment (row n = r), S^T (hi, lo) for the
         // next chunk
-        if (wait_own(inc_bar, c & 1, abort_flag) && issuer) inc_pend = false;
+        if (wait_own(inc_bar, c & 1, abort_flag) && issuer) pend &= ~kPINC;
         tc::fence_after();
         if (!issuer_warp) {
             const float eend = ex2(s2_end);
@@ -434,13 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) mma_pend = false;
+        if (wait_own(mma_bar, mma_phase, abort_flag) && issuer) pend &= ~kPMMA;
         mma_phase ^= 1u;
         tc::fence_after();
         if (issuer && c + 1 < nchunks && !*abort_flag) {   // B and X are free
             issue_bx(c + 1);
-            bx_pend = true;
-            bx_par = (c + 1) & 1;
+            set_pend(kPBX, (c + 1) & 1);
         }
 
         if (!issuer_warp) {
@@ -494,10 +505,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a wait gave up: record it and let this block's copies and products still in flight end (bounded;
         // products complete in order, so the last commit covers every earlier one)
         atomicOr(&g_ssd_wait_error, 1u);
-        if (c_pend) mbar_wait_bounded(bar_c, c_par);
-        if (bx_pend) mbar_wait_bounded(bar_bx, bx_par);
-        if (inc_pend) mbar_wait_bounded(inc_bar, inc_par);
-        if (mma_pend) mbar_wait_bounded(mma_bar, mma_par);
+        if (pend & kPC) mbar_wait_bounded(bar_c, (par & kPC) ? 1u : 0u);
+        if (pend & kPBX) mbar_wait_bounded(bar_bx, (par & kPBX) ? 1u : 0u);
+        if (pend & kPINC) mbar_wait_bounded(inc_bar, (par & kPINC) ? 1u : 0u);
+        if (pend & kPCS) mbar_wait_bounded(cs_bar, (par & kPCS) ? 1u : 0u);
+        if (pend & kPMMA) mbar_wait_bounded(mma_bar, (par & kPMMA) ? 1u : 0u);
     }
     if (issuer) bulk_wait_all();   // the y stores are complete
     tc::fence_before();
