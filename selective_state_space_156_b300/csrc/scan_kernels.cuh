@@ -95,7 +95,7 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
             const float dv_ = dtj * vj;
 #pragma unroll
             for (int n = 0; n < NS; ++n) {
-                float ab = ex2(dtj * cc.al2[n]);
+                const float ab = abar_exact(dtj * cc.al2[n]);
                 h[n] = fmaf(ab, h[n], dv_ * Bt[n]);
                 if (kFinal) {
                     if (n & 1) y1 = fmaf(Ct[n], h[n], y1);
@@ -105,9 +105,8 @@ __device__ __forceinline__ void scan_group(const ScanKernelArgs& a, const ScanSh
         } else {  // zero-order hold, exact form: Bbar = E B with E from zoh_factor (any a, a = 0 included)
 #pragma unroll
             for (int n = 0; n < NS; ++n) {
-                const float y = dtj * cc.al2[n];
-                const float ab = ex2(y);
-                const float E = zoh_factor(dtj, y, ab, cc.inva[n]);
+                float ab;
+                const float E = zoh_exact(dtj, dtj * cc.al2[n], cc.inva[n], ab);
                 h[n] = fmaf(ab, h[n], E * (Bt[n] * vj));
                 if (kFinal) {
                     if (n & 1) y1 = fmaf(Ct[n], h[n], y1);

@@ -75,6 +75,23 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Abar and E of the exact form together, for the kernels whose states carry fp32 accuracy over long
+// sequences (the fp32-output scan, the decode step): where the series holds, Abar = 1 + x phi(x) (x = y ln 2)
+// comes within about half an ulp of e^x, where the ~2 ulp of ex2.approx would build up over the thousands
+// of steps that such a state remembers; elsewhere 2^y and (2^y - 1) / a.  inva = 1 / a (0 where a == 0).
+__device__ __forceinline__ float zoh_exact(float dt, float y, float inva, float& ab) {
+    const float phi = zoh_phi_y(y);
+    const float e = ex2(y);
+    const bool series = fabsf(y) < kZohSeriesY;
+    ab = series ? fmaf(y * kLn2, phi, 1.0f) : e;
+    return series ? dt * phi : (e - 1.0f) * inva;
+}
+
+// Abar alone the same way, for the simplified input scale (Bbar = dt B) on those kernels.
+__device__ __forceinline__ float abar_exact(float y) {
+    return fabsf(y) < kZohSeriesY ? fmaf(y * kLn2, zoh_phi_y(y), 1.0f) : ex2(y);
+}
+
 // 1/x on the MUFU unit (rcp.approx.ftz: about 1 ulp).
 __device__ __forceinline__ float rcp(float x) {
     float y;

@@ -139,12 +139,12 @@ __global__ void __launch_bounds__(kDecThreads) state_update_kernel(const DecodeS
     for (int i = 0; i < NSL; ++i) {
         const float a = av[i];
         const float y = dt * (a * kLog2e);
-        const float ab = ex2(y);
-        if (kZOH) {  // exact form: E from the series where |dt a| < 2^-4, dt at a = 0
-            const float E = zoh_factor(dt, y, ab, a != 0.0f ? rcp(a) : 0.0f);
+        if (kZOH) {  // exact form: E (and Abar) from the series where |dt a| < 2^-4, dt at a = 0
+            float ab;
+            const float E = zoh_exact(dt, y, a != 0.0f ? rcp(a) : 0.0f, ab);
             h[i] = fmaf(ab, h[i], E * (uv * Bt[i]));
         } else {
-            h[i] = fmaf(ab, h[i], (dt * uv) * Bt[i]);
+            h[i] = fmaf(abar_exact(y), h[i], (dt * uv) * Bt[i]);
         }
         yp = fmaf(Ct[i], h[i], yp);
     }

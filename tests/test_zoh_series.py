@@ -162,3 +162,38 @@ def test_plain_quotient_fails_the_same_check():
         want = exact_E(dt, a)
         worst = max(worst, abs(float(got) - want) / abs(want))
     assert worst > 1e-2
+
+
+def device_Abar_series(dt, a):
+    """Abar as zoh_exact forms it where the series holds: 1 + x phi(x), x = y ln 2, one fmaf at the end."""
+    dt, a = f32(dt), f32(a)
+    y = f32(dt * f32(a * LOG2E))
+    p = fma32(y, PHI3, PHI2)
+    p = fma32(p, y, PHI1)
+    p = fma32(p, y, f32(1.0))
+    return fma32(f32(y * LN2), p, f32(1.0)), y
+
+
+LN2 = f32(0.6931471805599453)
+
+
+def test_series_Abar_is_within_an_ulp_of_exp():
+    """zoh_exact takes Abar from the series below the threshold (the fp32-output scan and the decode step):
+    within one ulp of e^x (of the fp32 x the device forms), where the hardware exp2 is allowed two; its
+    errors are also centred, so they do not add up over a long-memory state's thousands of steps."""
+    text = open(HEADER).read()
+    body = text[text.index("float zoh_exact("):]
+    body = body[:body.index("}")]
+    assert "fmaf(y * kLn2, phi, 1.0f)" in body and "fabsf(y) < kZohSeriesY" in body
+    errs = []
+    for dt, a in _grid():
+        got, y = device_Abar_series(dt, a)
+        if not abs(y) < SERIES_Y:
+            continue
+        want = math.exp(float(y) * math.log(2.0))
+        ulp = float(np.spacing(f32(want)))
+        errs.append((float(got) - want) / ulp)
+    errs = np.array(errs)
+    assert len(errs) > 300
+    assert np.abs(errs).max() <= 1.0, np.abs(errs).max()
+    assert abs(errs.mean()) < 0.1, errs.mean()
