@@ -401,16 +401,20 @@ ssm_status validate_bwd(const ssm_scan_bwd_params* p) {
     const size_t rows = (size_t)p->batch * p->dim, nbdl = rows * p->seqlen;
     const size_t eb = esize(p->in_dtype);
     const size_t nbnl = (size_t)p->batch * p->dstate * p->seqlen;
+    const size_t W = p->conv_w ? (size_t)p->conv_width : 0, W1 = W > 0 ? W - 1 : 0;  // conv taps, history
     struct Range { const void* p; size_t n; };
     const Range ins[] = {{p->u, nbdl * eb}, {p->delta, nbdl * eb}, {p->z, nbdl * eb}, {p->Bm, nbnl * eb},
                          {p->Cm, nbnl * eb}, {p->dy, nbdl * eb},
                          {p->h_ckpt, rows * (size_t)((p->seqlen + SSM_CKPT_STEPS - 1) / SSM_CKPT_STEPS) * p->dstate * 4},
-                         {p->A, (size_t)p->dim * p->dstate * 4}, {p->h0, rows * p->dstate * 4}};
+                         {p->A, (size_t)p->dim * p->dstate * 4}, {p->h0, rows * p->dstate * 4},
+                         {p->Dskip, (size_t)p->dim * 4}, {p->delta_bias, (size_t)p->dim * 4},
+                         {p->conv_w, (size_t)p->dim * W * 4}, {p->conv_b, W ? (size_t)p->dim * 4 : 0},
+                         {p->conv_init, rows * W1 * eb}, {p->dh_out, rows * p->dstate * 4}};
     const Range outs[] = {{p->du, nbdl * eb}, {p->ddelta, nbdl * eb}, {p->dz, nbdl * eb},
                           {p->dA, (size_t)p->dim * p->dstate * 4}, {p->dB, nbnl * 4}, {p->dC, nbnl * 4},
                           {p->dDskip, (size_t)p->dim * 4}, {p->ddelta_bias, (size_t)p->dim * 4},
-                          {p->dconv_w, (size_t)p->dim * 4 * 4}, {p->dconv_b, (size_t)p->dim * 4},
-                          {p->dh0, rows * p->dstate * 4}};
+                          {p->dconv_w, (size_t)p->dim * W * 4}, {p->dconv_b, W ? (size_t)p->dim * 4 : 0},
+                          {p->dconv_init, rows * W1 * eb}, {p->dh0, rows * p->dstate * 4}};
     for (const Range& o : outs) {
         if (!o.p) continue;
         for (const Range& i : ins)

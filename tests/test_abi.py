@@ -247,6 +247,28 @@ def test_bwd_rejects_bad_arguments_on_host(L):
     assert "overlaps" in L.ssm_last_error().decode()
 
 
+def test_bwd_checks_the_conv_gradients_for_overlaps(L):
+    """dconv_init (B, D, W - 1) and the conv inputs take part in the overlap checks, sized by the conv
+    width: an output inside dconv_init, or an output inside conv_w, is rejected before any launch."""
+    p = ssm.ScanBwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.in_dtype = 2, 64, 16, 128, ssm.SSM_BF16
+    fake = 1 << 40
+    for i, k in enumerate(["u", "delta", "A", "Bm", "Cm", "h_ckpt", "dy", "du", "ddelta", "dA", "dB", "dC"]):
+        setattr(p, k, fake + (i << 32))
+    p.delta_softplus, p.zoh = 1, 1
+    p.conv_w, p.conv_width = fake + (30 << 32), 2
+    p.conv_init = fake + (31 << 32)
+    p.dconv_w, p.dconv_b = fake + (32 << 32), fake + (34 << 32)
+    p.dconv_init = fake + (33 << 32)
+    p.du = p.dconv_init + 2 * 64 * 1 * 2 - 2       # the last element of dconv_init (bf16, (2, 64, 1))
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "two outputs overlap" in L.ssm_last_error().decode()
+    p.du = fake + (7 << 32)
+    p.dconv_b = p.conv_w + 64 * 2 * 4 - 4          # the last tap of conv_w (fp32, (64, 2))
+    assert L.ssm_scan_bwd(ctypes.byref(p), None) == ssm.SSM_ERR_INVALID_ARG
+    assert "an output overlaps an input" in L.ssm_last_error().decode()
+
+
 def test_ssd_params_struct_layout_matches_c():
     got = _c_layout("ssd_scan_params", """
   F(batch) F(nheads) F(headdim) F(ngroups) F(dstate) F(seqlen) F(x) F(dt) F(A) F(Bm) F(Cm) F(Dskip) F(dt_bias)

@@ -90,6 +90,19 @@ def test_backward_matches_oracle(dt, N, D, L, flags):
     _compare(d, grads, ref, d["u"].dtype)
 
 
+@pytest.mark.parametrize("W", [1, 2, 3])
+def test_backward_conv_widths(W):
+    """Filters narrower than 4 taps ((D, W) taps and their gradient, W - 1 steps of history)."""
+    d = _inputs(2, 96, 8, 72, "bf16", 9500 + W)
+    d["conv_w"] = d["conv_w"][:, 4 - W:].contiguous()
+    d["conv_init"] = d["conv_init"][..., 4 - W:].contiguous() if W > 1 else None
+    gen = torch.Generator().manual_seed(9600 + W)
+    dy = torch.randn((2, 96, 72), generator=gen).to(torch.bfloat16)
+    grads, dyr = _run(d, dy)
+    ref = obwd.scan_bwd(d, dyr)
+    _compare(d, grads, ref, torch.bfloat16)
+
+
 def test_backward_at_the_layer_shape_sampled():
     """The Mamba-1.4B layer with its fused front end (8 x 4096 x 16 x 2048, bf16): per-row gradients on 6
     sampled rows (each row's oracle is the same problem cut to that row), per-channel sums (dA, D skip, dt
