@@ -303,16 +303,16 @@ __global__ void __launch_bounds__(kBulkThreads + 32, 4) state_update_bulk_kernel
     #pragma unroll
                     for (int i = 0; i < SL; ++i) {
                         const float y = dt * (A4[i] * kLog2e);
-                        float ab = ex2(y);
                         if (kZOH && kExact) {
                             // exact form, branch-free: E (and Abar) from the series where |dt a| < 2^-4 (dt at
                             // a = 0)
+                            float ab;
                             const float E = zoh_exact(dt, y, A4[i] != 0.0f ? rcp(A4[i]) : 0.0f, ab);
                             h[i] = fmaf(ab, h[i], E * (uv * Bv[i]));
                         } else if (kZOH) {
                             // fast form h' = Abar (h - ng) + ng, ng = -(v / a) B (every |a| >= 1/4 in the warp)
                             const float ng = (uv * -rcp(A4[i])) * Bv[i];
-                            h[i] = fmaf(ab, h[i] - ng, ng);
+                            h[i] = fmaf(ex2(y), h[i] - ng, ng);
                         } else {
                             h[i] = fmaf(abar_exact(y), h[i], dtu * Bv[i]);
                         }
