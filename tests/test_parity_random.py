@@ -1,6 +1,7 @@
 """Randomised parity cases through the C ABI: fixed seeds draw shapes, dtypes and flags for the scan
-forward, the backward pass, the decode step and the SSD layer, and each case is compared with the oracle
-at the stated bounds (the scan and decode on up to 48 sampled rows).
+forward, the backward pass, the decode step, the SSD layer and the state-slot paths of the scan and the
+decode step, and each case is compared with the oracle at the stated bounds (the scan and decode on up to
+48 sampled rows).
 
 Ragged channel counts and lengths, every state size the dispatch distinguishes (1 to 16, 32, 64), fp32
 and bf16 inputs and outputs, conv widths 1 to 4 with and without history, gate, D skip, dt bias, softplus
@@ -214,3 +215,73 @@ def test_random_ssd_cases(block):
         _check_y(y, ref_y.reshape(y.shape), f"case {i} y")
         r = _ratio(h, ref_h.reshape(h.shape), h_tolerance(ref_h.reshape(h.shape), torch.bfloat16))
         assert r <= 1.0, f"case {i}: h_out at {r:.3f} of the bound"
+
+
+@pytest.mark.parametrize("block", range(2))
+def test_random_slot_cases(block):
+    """Scan and decode on per-request state slots (state_indices): random batch-to-slot maps with padding
+    rows, conv widths 0 to 4 with the conv history kept in a slot cache too; unused slots must come back
+    bit-identical and a padding row's y zero."""
+    rng = random.Random(7500 + block)
+    for i in range(40):
+        seed = rng.randint(0, 10**9)
+        g = torch.Generator().manual_seed(seed)
+        Bsz = rng.randint(1, 9)
+        S = Bsz + rng.randint(0, 6)
+        D, N = rng.choice([rng.randint(1, 200), 8 * rng.randint(1, 40)]), rng.randint(1, 16)
+        L = rng.choice([1, rng.randint(1, 40), rng.randint(41, 600)])
+        dt, W, which = rng.choice(["f32", "bf16"]), rng.choice([0, 0, 1, 2, 3, 4]), rng.choice(["scan", "decode"])
+        idx = torch.tensor([s if rng.random() > 0.2 else -1 for s in rng.sample(range(S), Bsz)], dtype=torch.int32)
+        d = workloads.make_scan_inputs(workloads.ScanConfig("slots", Bsz, D, N, L, dt, conv=W > 0, seed=seed % 100000))
+        if W:
+            d["conv_w"] = d["conv_w"][:, 4 - W:].contiguous()
+        idt = d["u"].dtype
+        cache = torch.randn((S, D, N), generator=g) * 0.5
+        cc = torch.randn((S, D, W - 1), generator=g).to(idt) if W > 1 else None
+        cache_d, cc_d = cache.cuda(), (cc.cuda() if cc is not None else None)
+        live = [b for b in range(Bsz) if idx[b] >= 0]
+        li = idx[live].long()
+        what = f"case {i} ({which}, B {Bsz}, S {S}, D {D}, N {N}, L {L}, {dt}, W {W}, slots {idx.tolist()})"
+        if which == "scan":
+            gd = {k: (v.cuda().contiguous() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+            y = ssm.ssm_scan_fwd(gd["u"], gd["delta"], gd["A"], gd["Bm"], gd["Cm"], Dskip=gd["Dskip"],
+                                 delta_bias=gd["delta_bias"], z=gd["z"], conv_w=gd.get("conv_w"),
+                                 conv_b=gd.get("conv_b"), h0=cache_d, h_out=cache_d, state_indices=idx.cuda(),
+                                 conv_init=cc_d, conv_final=cc_d)
+            torch.cuda.synchronize()
+            if live:
+                sub = {k: (v[live] if isinstance(v, torch.Tensor) and v.dim() == 3 and v.shape[0] == Bsz else v)
+                       for k, v in d.items()}
+                sub["h0"] = cache[li]
+                if cc is not None:
+                    sub["conv_init"] = cc[li]
+                yr, hr, _ = oracle.scan(sub)
+                yr, hr = yr.reshape(len(live), D, L), hr.reshape(len(live), D, N)
+                assert _ratio(y[live], yr, y_tolerance(yr, idt)) <= 1.0, what + ": y"
+                assert _ratio(cache_d.cpu()[li], hr, h_tolerance(hr, idt)) <= 1.0, what + ": slot states"
+            assert all(bool((y[b] == 0).all()) for b in range(Bsz) if idx[b] < 0), what + ": padding y"
+            if cc is not None:
+                for b in live:
+                    want = torch.cat([cc[int(idx[b])], d["u"][b]], dim=-1)[:, -(W - 1):]
+                    assert torch.equal(cc_d.cpu()[int(idx[b])], want), what + ": conv history"
+        else:
+            x, de, z = (d[k][..., 0].contiguous() for k in ("u", "delta", "z"))
+            Bm, Cm = d["Bm"][..., 0].contiguous(), d["Cm"][..., 0].contiguous()
+            y = ssm.ssm_state_update(cache_d, x.cuda(), de.cuda(), d["A"].cuda(), Bm.cuda(), Cm.cuda(),
+                                     Dskip=d["Dskip"].cuda(), delta_bias=d["delta_bias"].cuda(), z=z.cuda(),
+                                     conv_w=d["conv_w"].cuda() if W else None,
+                                     conv_b=d["conv_b"].cuda() if W else None, conv_state=cc_d,
+                                     state_indices=idx.cuda())
+            torch.cuda.synchronize()
+            if live:
+                kw = dict(conv_w=d["conv_w"], conv_b=d["conv_b"],
+                          conv_state=cc[li] if cc is not None else None) if W else {}
+                out = oracle.state_update(cache[li], x[live], de[live], d["A"], Bm[live], Cm[live], d["Dskip"],
+                                          d["delta_bias"], z[live], **kw)
+                assert _ratio(y[live], out[1], y_tolerance(out[1], idt)) <= 1.0, what + ": y"
+                assert _ratio(cache_d.cpu()[li], out[0], h_tolerance(out[0], idt)) <= 1.0, what + ": slot states"
+        unused = sorted(set(range(S)) - set(li.tolist()))
+        assert torch.equal(cache_d.cpu()[unused], cache[unused]), what + ": an unused slot changed"
+        if cc is not None:
+            assert torch.equal(cc_d.cpu()[unused], cc[unused]), what + ": an unused conv slot changed"
+        assert ssm.ssm_device_error() == 0
