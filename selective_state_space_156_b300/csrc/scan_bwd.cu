@@ -102,18 +102,25 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
     // per-channel constants, as packed pairs of states (n, n + 1)
     // (the exponent argument dt a log2 e is formed as (dt log2 e) a, one scalar product per step)
     f32x2 a2[NS / 2], inva2[NS / 2];
+    bool small_a = false;   // some state of this channel with |A| < kZohFastMinA (0 included)
 #pragma unroll
     for (int p = 0; p < NS / 2; ++p) {
         float av[2], iv[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int n = 2 * p + q;
-            av[q] = (active && n < N) ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
+            const bool real = active && n < N;
+            av[q] = real ? __ldg(a.A + (size_t)dd * N + n) : 0.0f;
             iv[q] = av[q] != 0.0f ? 1.0f / av[q] : 0.0f;
+            small_a |= real && !(fabsf(av[q]) >= kZohFastMinA);
         }
         a2[p] = pack2(av[0], av[1]);
         inva2[p] = pack2(iv[0], iv[1]);
     }
+    // Block-uniform: with bf16 inputs and every |A| of the block at least kZohFastMinA, the forward pass
+    // took the fast form h' = Abar (h - ng) + ng, ng = -(v / a) B; the recomputation of a group's states
+    // takes it too (fewer products than the exact E, and the same rounding as the forward's states).
+    const bool fast_rc = kZOH && Tin::kBytes == 2 && !__syncthreads_or(small_a);
     float w[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb = 0.0f;
     if (kConv && active) {
         const int W = a.conv_width;
@@ -315,13 +322,22 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const ScanBwdArgs
                     const f32x2 dt2 = pack2(dtv[j], dtv[j]), v2 = pack2(vv[j], vv[j]);
                     const float dtl = dtv[j] * kLog2e;
                     const f32x2 dtl2 = pack2(dtl, dtl);
+                    if (fast_rc) {
 #pragma unroll
-                    for (int p = 0; p < NS / 2; ++p) {
-                        const f32x2 y2 = mul2(dtl2, a2[p]);
-                        const f32x2 Ab = ex2x2(y2);
-                        f32x2 E = dt2;
-                        if (kZOH) E = zoh_e2(dt2, y2, Ab, inva2[p]);
-                        hcur[p] = fma2(Ab, hcur[p], mul2(E, mul2(v2, Bt[p])));
+                        for (int p = 0; p < NS / 2; ++p) {
+                            const f32x2 Ab = ex2x2(mul2(dtl2, a2[p]));
+                            const f32x2 q = mul2(mul2(v2, inva2[p]), Bt[p]);   // -ng = (v / a) B
+                            hcur[p] = fma2(Ab, add2(hcur[p], q), mul2(q, pack2(-1.0f, -1.0f)));
+                        }
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) {
+                            const f32x2 y2 = mul2(dtl2, a2[p]);
+                            const f32x2 Ab = ex2x2(y2);
+                            f32x2 E = dt2;
+                            if (kZOH) E = zoh_e2(dt2, y2, Ab, inva2[p]);
+                            hcur[p] = fma2(Ab, hcur[p], mul2(E, mul2(v2, Bt[p])));
+                        }
                     }
                     if (j == kBwdGroup - 1) break;  // the group's last state stays in hcur
 #pragma unroll
